@@ -1,0 +1,528 @@
+"""Benchmark of the ISD verify/accept step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload isd_c64_n4_ctx4096]
+
+One step = the whole hot path over one batch: paged strict-causal attention of
+the 2N-1 rows of every request against its KV cache, the accept pass (softmax
+statistics, p/q test, residual / bonus draw, proposals, next state) and the KV
+commit of the accepted rows.  The default workload is C=64 requests, N=4,
+4096-token contexts, 32/8 heads of 128, V=151936: synthetic, seeded inputs of
+those shapes.  Every step reads ~1.08 GB of KV and 136 MB of logits, more than
+the 126 MB L2, so no explicit flush is needed between steps.
+
+The metric is emitted tokens per second (accepted drafts plus the resampled,
+bonus or fresh token of each request, the numerator of the pages' tokens per
+forward).  Under torchrun each rank runs its own batch (replicas, weak
+scaling); the reported value is all ranks' tokens over the slowest rank's
+time.  Prints one JSON line (rank 0).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "ISD accepted tokens/s at C=64,N=4; attention+accept HBM GB/s vs B300 peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="isd_c64_n4_ctx4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+def source_hash(name):
+    path = os.path.join(ROOT, "speculative_verify_accept_step_b300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_file, workload):
+    """Per-launch DRAM bytes from the committed ncu summary, if still current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel_file, {}).get(workload)
+    if not e or e.get("source_sha") != source_hash(kernel_file):
+        return None
+    return e.get("bytes_per_launch")
+
+
+# --------------------------------------------------------------- dist helpers
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce(x, ws, op):
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=op)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- clock sampling
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"isd_clocks_{os.getpid()}.csv")
+        self.idx = device_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class Step:
+    """Device buffers of one ISD step and the three C-ABI calls that run it."""
+
+    def __init__(self, w, dev, seed=0):
+        import speculative_verify_accept_step_b300 as L
+        from speculative_verify_accept_step_b300 import workloads as wl
+        self.L, self.w, self.dev = L, w, dev
+        a = wl.attention_inputs(w, seed=seed)
+        b = wl.accept_inputs(w, seed=seed)
+        self.host = dict(a=a, b=b)
+        d = lambda t: t.to(dev)
+        self.q, self.k_new, self.v_new = d(a["q"]), d(a["k_new"]), d(a["v_new"])
+        self.k_cache, self.v_cache = d(a["k_cache"]), d(a["v_cache"])
+        self.page_table, self.seq_lens, self.qo = d(a["page_table"]), d(a["seq_lens"]), d(a["qo_indptr"])
+        self.sm_scale = a["sm_scale"]
+        self.logits0, self.logits1 = d(b["logits0"]), d(b["logits1"])
+        self.qo0, self.qo1 = d(b["qo0"]), d(b["qo1"])
+        C, N, T = w.C, w.N, w.T
+        M = N - 1
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.att_ws = torch.empty(max(L.idlm_isd_attention_workspace_size(
+            C, w.Hq, w.Hkv, w.D, w.page_size, w.rows_full, L.IDLM_BF16), 256),
+            dtype=torch.uint8, device=dev)
+        V = w.V
+        self.acc_ws = torch.empty(L.idlm_isd_accept_workspace_size(C, max(T, C * N), N, V),
+                                  dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, **i32)
+        self.seq_out = torch.empty_like(self.seq_lens)
+        self.releasable = torch.empty_like(self.seq_lens)
+
+        def outs():
+            return dict(n_accepted=torch.empty(C, **i32), out_tokens=torch.empty((C, N), **i32),
+                        n_out=torch.empty(C, **i32), n_commit=torch.empty(C, **i32),
+                        next_drafts=torch.empty((C, M), **i32),
+                        next_q_stats=torch.empty((C, M, 2), dtype=torch.float32, device=dev),
+                        next_mode=torch.empty(C, dtype=torch.uint8, device=dev),
+                        next_mask_row0=torch.empty(C, **i32))
+        self.outs = outs
+        # step 0 (FRESH): the MASK rows of logits0 propose the drafts verified by every
+        # timed FULL step
+        s0 = outs()
+        L.idlm_isd_accept(self.logits0, self.qo0, d(b["mode0"]),
+                          torch.full((C, M), -1, **i32),
+                          torch.zeros((C, M, 2), dtype=torch.float32, device=dev), self.logits0,
+                          torch.zeros(C, **i32), N, w.temperature, L.PROPOSE_ARGMAX, 0, 0,
+                          s0["n_accepted"], s0["out_tokens"], s0["n_out"], s0["n_commit"],
+                          s0["next_drafts"], s0["next_q_stats"], s0["next_mode"],
+                          s0["next_mask_row0"], self.acc_ws, self.status)
+        self.mode1, self.drafts, self.dq, self.prow = (s0["next_mode"], s0["next_drafts"],
+                                                       s0["next_q_stats"], s0["next_mask_row0"])
+        torch.cuda.synchronize()
+
+    def attention(self):
+        self.L.idlm_isd_attention(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                  self.page_table, self.seq_lens, self.qo, self.out, self.att_ws,
+                                  self.status, max_rows=self.w.rows_full, sm_scale=self.sm_scale)
+
+    def accept(self, o, step, logits=None):
+        L, w = self.L, self.w
+        L.idlm_isd_accept(self.logits1 if logits is None else logits, self.qo1, self.mode1,
+                          self.drafts, self.dq, self.logits0, self.prow, w.N, w.temperature,
+                          L.PROPOSE_ARGMAX, 0, step, o["n_accepted"], o["out_tokens"],
+                          o["n_out"], o["n_commit"], o["next_drafts"], o["next_q_stats"],
+                          o["next_mode"], o["next_mask_row0"], self.acc_ws, self.status)
+
+    def commit(self, o):
+        self.L.idlm_kv_commit(self.k_cache, self.v_cache, self.page_table, self.seq_lens,
+                              self.seq_out, self.k_new, self.v_new, self.qo, o["n_commit"],
+                              self.status, releasable_from=self.releasable)
+
+
+def attention_bytes(w, seq_lens):
+    """Algorithmic HBM bytes of one attention launch: every cached K/V byte
+    read once, Q and the new K/V rows read once, the output written once, and
+    the page-table entries read."""
+    el = 2 if w.dtype == "bf16" else 4
+    kv = int(seq_lens.sum()) * w.Hkv * w.D * el * 2
+    q = w.T * w.Hq * w.D * el
+    new = w.T * w.Hkv * w.D * el * 2
+    out = w.T * w.Hq * w.D * el
+    pages = sum((int(L) + w.page_size - 1) // w.page_size for L in seq_lens) * 4
+    return kv + q + new + out + pages
+
+
+def accept_bytes(w, n_rejected):
+    """Algorithmic HBM bytes of one accept call: every logit row read once,
+    plus the p_j and q_j rows re-read for each rejected request."""
+    el = 2 if w.dtype == "bf16" else 4
+    return w.T * w.V * el + n_rejected * 2 * w.V * el
+
+
+def run_ours(args):
+    from speculative_verify_accept_step_b300 import workloads as wl
+    rank, ws, local = dist_init()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]
+    st = Step(w, dev, seed=rank)
+    K, Wm = args.steps, args.warmup
+    outs = [st.outs() for _ in range(K)]
+    wo = st.outs()
+    for i in range(Wm):
+        st.attention()
+        st.accept(wo, 10_000_000 + i)
+        st.commit(wo)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    # keep the GPU loaded for ~0.6 s while the sampler starts, so its readings
+    # before the timed region are taken under the same load
+    t_load = time.time()
+    i = 0
+    while time.time() - t_load < 0.6:
+        for _ in range(50):
+            st.attention()
+            st.accept(wo, 20_000_000 + i)
+            st.commit(wo)
+            i += 1
+        torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record()
+    for k in range(K):
+        ev[k][0].record()
+        st.attention()
+        ev[k][1].record()
+        st.accept(outs[k], k + 1)
+        ev[k][2].record()
+        st.commit(outs[k])
+        ev[k][3].record()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_local = e0.elapsed_time(e1)
+    ms = allreduce(ms_local, ws, _max_op())
+    assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
+    n_out = torch.stack([o["n_out"] for o in outs]).sum().item()
+    n_acc = torch.stack([o["n_accepted"] for o in outs]).sum().item()
+    n_rej = torch.stack([(o["next_mode"] == 0).sum() for o in outs]).sum().item()
+    tokens = allreduce(float(n_out), ws, _sum_op())
+    att_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    acc_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    com_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    hbm, bf16, peak_kind = peaks()
+    a_bytes = attention_bytes(w, st.host["a"]["seq_lens"])
+    c_bytes = accept_bytes(w, n_rej / K)
+    att_gbs = a_bytes / (att_ms * 1e-3) / 1e9
+    acc_gbs = c_bytes / (acc_ms * 1e-3) / 1e9
+    both_gbs = (a_bytes + c_bytes) / ((att_ms + acc_ms) * 1e-3) / 1e9
+
+    e2e = run_e2e(st, args.e2e_steps, ws)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, st.host)
+    if rank != 0:
+        return
+    traffic = ncu_traffic("attention.cu", w.name)
+    line = {
+        "metric": METRIC,
+        "value": tokens / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the workload)",
+        "config": {"workload": w.name, "C": w.C, "N": w.N, "context": w.ctx_lo if w.ctx == "fixed"
+                   else f"{w.ctx} [{w.ctx_lo}, {w.ctx_hi}]", "heads": f"{w.Hq}/{w.Hkv}",
+                   "head_dim": w.D, "page_size": w.page_size, "V": w.V,
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (KV %.2f GB + logits %.0f MB read per step)"
+                         % (a_bytes / 1e9, w.T * w.V * 2 / 1e6)},
+        "roofline": {"bound": "hbm", "kernel": "paged_attn_kernel (idlm_isd_attention)",
+                     "achieved": att_gbs, "peak": hbm, "unit": "GB/s", "frac": att_gbs / hbm,
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": a_bytes},
+        "kernels": {
+            "attention": {"us": att_ms * 1e3, "GB/s": att_gbs, "frac": att_gbs / hbm},
+            "accept": {"us": acc_ms * 1e3, "GB/s": acc_gbs, "frac": acc_gbs / hbm,
+                       "algorithmic_bytes": c_bytes},
+            "commit": {"us": com_ms * 1e3},
+            "attention+accept": {"GB/s": both_gbs, "frac": both_gbs / hbm},
+        },
+        "tokens_per_step": n_out / K,
+        "accepted_drafts_per_step": n_acc / K,
+        "accepted_drafts_per_s": allreduce(float(n_acc), ws, _sum_op()) / (ms * 1e-3),
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+def _max_op():
+    import torch.distributed as dist
+    return dist.ReduceOp.MAX
+
+
+def _sum_op():
+    import torch.distributed as dist
+    return dist.ReduceOp.SUM
+
+
+def run_e2e(st, K, ws):
+    """Same metric through the C ABI with host buffers: every step copies its
+    inputs (Q, new K/V rows, logits, layout and draft state) from pinned host
+    memory and reads the emitted tokens back."""
+    a, b = st.host["a"], st.host["b"]
+    pin = lambda t: t.pin_memory()
+    h = dict(q=pin(a["q"]), k_new=pin(a["k_new"]), v_new=pin(a["v_new"]),
+             logits=pin(b["logits1"]), page_table=pin(a["page_table"]),
+             seq_lens=pin(a["seq_lens"]), qo=pin(a["qo_indptr"]),
+             mode=pin(st.mode1.cpu()), drafts=pin(st.drafts.cpu()), dq=pin(st.dq.cpu()),
+             prow=pin(st.prow.cpu()))
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    o = st.outs()
+    back = {k: torch.empty(o[k].shape, dtype=o[k].dtype).pin_memory()
+            for k in ("out_tokens", "n_out", "next_drafts", "next_mode")}
+    d2h = sum(t.numel() * t.element_size() for t in back.values())
+    dev_logits = torch.empty_like(st.logits1)
+    tokens = 0
+    for rep in range(2):   # one untimed pass, then the timed one
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in range(K):
+            st.q.copy_(h["q"], non_blocking=True)
+            st.k_new.copy_(h["k_new"], non_blocking=True)
+            st.v_new.copy_(h["v_new"], non_blocking=True)
+            dev_logits.copy_(h["logits"], non_blocking=True)
+            st.page_table.copy_(h["page_table"], non_blocking=True)
+            st.seq_lens.copy_(h["seq_lens"], non_blocking=True)
+            st.qo.copy_(h["qo"], non_blocking=True)
+            st.mode1.copy_(h["mode"], non_blocking=True)
+            st.drafts.copy_(h["drafts"], non_blocking=True)
+            st.dq.copy_(h["dq"], non_blocking=True)
+            st.prow.copy_(h["prow"], non_blocking=True)
+            st.attention()
+            st.accept(o, 30_000_000 + k, logits=dev_logits)
+            st.commit(o)
+            for key, t in back.items():
+                t.copy_(o[key], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            if rep:
+                tokens += int(back["n_out"].sum())
+        e1.record()
+        torch.cuda.synchronize()
+    ms = allreduce(e0.elapsed_time(e1), ws, _max_op())
+    tokens = allreduce(float(tokens), ws, _sum_op())
+    return {"value": tokens / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K}
+
+
+# ------------------------------------------------------------- CPU baseline
+
+def _oracle_step(host, w, requests, step):
+    """The oracle's full step for a subset of requests; returns tokens emitted."""
+    import numpy as np
+    from oracle import isd
+    a, b = host["a"], host["b"]
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    qo = a["qo_indptr"].numpy()
+    M = w.N - 1
+    kc, vc = a["k_cache"], a["v_cache"]
+    emitted = 0
+    for c in requests:
+        t0, t1 = qo[c], qo[c + 1]
+        pages = a["page_table"][c]
+        used = pages[pages >= 0].long()
+        # gather only this request's pages for the oracle
+        remap = torch.full((int(a["num_pages"]),), -1, dtype=torch.long)
+        remap[used] = torch.arange(used.numel())
+        table = np.where(pages.numpy() >= 0, remap[pages.clamp(min=0).long()].numpy(), -1)
+        isd.isd_attention(f64(a["q"][t0:t1]), f64(a["k_new"][t0:t1]), f64(a["v_new"][t0:t1]),
+                          f64(kc[used]), f64(vc[used]), table[None], a["seq_lens"][c:c + 1].numpy(),
+                          np.array([0, t1 - t0]), w.page_size, a["sm_scale"])
+        r0 = b["qo0"][c].item()
+        r1 = b["qo1"][c].item()
+        l0 = f64(b["logits0"][r0:r0 + w.N])
+        l1 = f64(b["logits1"][r1:r1 + 2 * w.N - 1])
+        o0 = isd.isd_accept(l0, np.array([0, w.N]), np.array([isd.FRESH]), np.full((1, M), -1),
+                            l0, np.zeros(1, dtype=np.int64), w.N, w.temperature,
+                            isd.PROPOSE_ARGMAX, 0, 0, request_ids=np.array([c]))
+        o1 = isd.isd_accept(l1, np.array([0, 2 * w.N - 1]), o0["next_mode"], o0["next_drafts"],
+                            l0, o0["next_mask_row0"], w.N, w.temperature, isd.PROPOSE_ARGMAX, 0,
+                            step, request_ids=np.array([c]))
+        n = int(o1["n_commit"][0])
+        isd.kv_commit(f64(kc[used]), f64(vc[used]), table[None], a["seq_lens"][c:c + 1].numpy(),
+                      f64(a["k_new"][t0:t1]), f64(a["v_new"][t0:t1]), np.array([0, t1 - t0]),
+                      np.array([n]), w.page_size)
+        emitted += int(o1["n_out"][0])
+    return emitted
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        return 1
+
+
+def cpu_baseline(w, host, budget_s=15.0):
+    """The oracle as it stands, on a bounded sample of the same batch."""
+    t0 = time.time()
+    tokens, req, step = 0, 0, 1
+    while time.time() - t0 < budget_s and req < w.C:
+        tokens += _oracle_step(host, w, [req], step)
+        req += 1
+    dt = time.time() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"full step (attention, accept, commit) for {req} of {w.C} requests, "
+                      f"{dt:.1f} s, numpy float64"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from speculative_verify_accept_step_b300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    host = dict(a=wl.attention_inputs(w), b=wl.accept_inputs(w))
+    per_step = 1     # requests per reference step: a bounded sample of the batch
+    for i in range(args.warmup):
+        _oracle_step(host, w, [i % w.C], i + 1)
+    t0 = time.time()
+    tokens = 0
+    done = 0
+    for k in range(args.steps):
+        tokens += _oracle_step(host, w, [(k * per_step) % w.C], k + 1)
+        done += 1
+        if time.time() - t0 > 150.0:   # keep the whole run within a few minutes
+            break
+    dt = time.time() - t0
+    v = tokens / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": done, "steps_requested": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / done * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes of the workload)",
+        "config": {"workload": w.name, "C": w.C, "N": w.N, "V": w.V},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+                         "sample": f"one request of {w.C} per step (full step: attention, "
+                                   "accept, commit), numpy float64"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    sys.path.insert(0, ROOT)
+    if args.impl == "reference":
+        return run_reference(args)
+    from speculative_verify_accept_step_b300.build import build
+    if not os.path.exists(os.path.join(ROOT, "speculative_verify_accept_step_b300", "libidlm.so")):
+        build()
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

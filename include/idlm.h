@@ -1,0 +1,232 @@
+/*
+ * idlm.h -- C ABI of the Introspective Strided Decoding (ISD) step on B300.
+ *
+ * One ISD step of an Introspective Diffusion Language Model proposes new
+ * tokens at MASK positions (distribution q) and verifies the previous step's
+ * proposals at clean positions (anchor distribution p) in one forward pass,
+ * keeping a draft x with probability min(1, p(x)/q(x)).  Sources, cited by
+ * title and section:
+ *   [IDLM] "Introspective Diffusion Language Models" (project page):
+ *          "Inference & ISD", "Serving (SGLang)", "Lossless R-ISD",
+ *          "Training", "How do DLMs perform as they approach compute-bound?".
+ *   [GN]   "I-DLM - Icgozlemsel Difuzyon Dil Modelleri" (GeekNews summary):
+ *          "I-DLM Yontemi", "Inference & ISD", "Speedup Factor Explorer".
+ *
+ * Row layout of a request inside a step (rows are consecutive, the request's
+ * first row is qo_indptr[c]):
+ *   FULL  (mode 1): N clean rows [anchor, d_1 .. d_{N-1}] then N-1 MASK rows
+ *                   (2N-1 rows; [IDLM] "How do DLMs perform ...": 2N-1
+ *                   queries per forward).  Clean row i-1 verifies draft d_i;
+ *                   clean row N-1 gives the bonus slot; MASK row k proposes
+ *                   the next step's draft k.
+ *   FRESH (mode 0): 1 clean row [anchor] then N-1 MASK rows (N rows), used
+ *                   after a rejection.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is DEVICE memory owned by the caller, unless the
+ *     comment says otherwise.  The library allocates nothing and keeps no
+ *     state between calls.
+ *   - Tensors are dense row-major ("C order") with the shapes given.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream).  They launch kernels and, where stated, one
+ *     cudaMemsetAsync of the workspace; nothing else.
+ *   - The return value reports what the host can check before launching
+ *     (argument ranges, workspace size, unsupported shapes) and launch
+ *     errors.  On a non-OK return nothing was launched, except for
+ *     IDLM_ERR_CUDA, which reports a failed launch.
+ *   - Errors that depend on device data (a page id outside the pool, a token
+ *     id outside the vocabulary, a row layout that disagrees with `mode`, a
+ *     wait that ran out) are written to the caller's device word `status`
+ *     (int32, one per call, set to 0 by the caller beforehand): the first
+ *     error code wins (atomicCAS).  Kernels never trap.  Outputs of a call
+ *     that set `status` are unspecified, but no memory outside the buffers
+ *     passed in is written.
+ *   - `workspace` is caller-owned device scratch of at least the size the
+ *     matching *_workspace_size() query returns, 256-byte aligned.  Its
+ *     contents need no initialisation.  A workspace must not be shared by
+ *     calls that may run concurrently.
+ */
+#ifndef IDLM_H
+#define IDLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  IDLM_OK = 0,
+  IDLM_ERR_INVALID_ARG = 1,   /* a pointer, size or enum out of range */
+  IDLM_ERR_UNSUPPORTED = 2,   /* valid but not implemented (dtype, D, group) */
+  IDLM_ERR_WORKSPACE = 3,     /* workspace missing or too small */
+  IDLM_ERR_CUDA = 4           /* a CUDA runtime call or launch failed */
+} idlm_status;
+
+/* Codes written to the device `status` word. */
+#define IDLM_DEV_OK 0
+#define IDLM_DEV_BAD_PAGE 1     /* page id outside [0, num_pages) */
+#define IDLM_DEV_BAD_TOKEN 2    /* draft token outside [0, V) */
+#define IDLM_DEV_BAD_LAYOUT 3   /* rows of a request disagree with its mode */
+#define IDLM_DEV_SLOT_OVERFLOW 4 /* a slot beyond the request's page table */
+#define IDLM_DEV_TIMEOUT 5      /* a bounded wait inside a kernel ran out */
+
+/* Element types. */
+#define IDLM_F32 0
+#define IDLM_BF16 1
+
+/* Request modes and proposal modes. */
+#define IDLM_MODE_FRESH 0
+#define IDLM_MODE_FULL 1
+#define IDLM_PROPOSE_ARGMAX 0
+#define IDLM_PROPOSE_SAMPLE 1
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int idlm_version(void);
+
+/* Static text for a status code. */
+const char* idlm_status_string(int status);
+
+/* ------------------------------------------------------------------------
+ * a2. Paged strict-causal GQA attention of the step rows.
+ *
+ * [IDLM] "Training" (strict causal masking across all positions) and
+ * "Serving (SGLang)" (paged KV cache, paged-only attention kernel).
+ * Row r of request c sits at position L_c + r (L_c = seq_lens[c]) and
+ * attends to the committed slots 0 .. L_c-1, read through
+ * page_table[c][slot / page_size] at offset slot % page_size, and to this
+ * step's new K/V rows 0 .. r of the same request.  Query head h reads KV head
+ * h / (Hq / Hkv).  out = softmax(q k^T * sm_scale) v, accumulated in fp32.
+ *
+ *   q          [T, Hq, D]              this step's query rows
+ *   k_new      [T, Hkv, D]             this step's keys (not yet cached)
+ *   v_new      [T, Hkv, D]
+ *   k_cache    [num_pages, Hkv, page_size, D]
+ *   v_cache    [num_pages, Hkv, page_size, D]
+ *   page_table [C, max_pages] int32   physical page of each logical page
+ *   seq_lens   [C] int32               committed length L_c (read only)
+ *   qo_indptr  [C+1] int32             first row of each request; qo_indptr[C] = T
+ *   out        [T, Hq, D]              written for every row
+ *   dtype      IDLM_BF16 or IDLM_F32 for q, k_*, v_*, caches and out
+ *   max_rows   upper bound on qo_indptr[c+1]-qo_indptr[c] (e.g. 2N-1)
+ * Fast path: dtype BF16, D = 128, page_size = 16, (Hq/Hkv) * max_rows <= 64
+ * (a TMA-fed tensor-core kernel); other shapes run a simple CUDA-core kernel
+ * (any page_size, D a multiple of 32 up to 256).  Device errors: BAD_PAGE,
+ * BAD_LAYOUT (a request with more than max_rows rows), TIMEOUT.
+ * Workspace: idlm_isd_attention_workspace_size(); it depends on the current
+ * device's SM count.
+ * ---------------------------------------------------------------------- */
+size_t idlm_isd_attention_workspace_size(int C, int Hq, int Hkv, int D,
+                                         int page_size, int max_rows, int dtype);
+
+idlm_status idlm_isd_attention(
+    const void* q, const void* k_new, const void* v_new,
+    const void* k_cache, const void* v_cache,
+    const int32_t* page_table, int max_pages,
+    const int32_t* seq_lens, const int32_t* qo_indptr,
+    int C, int T, int Hq, int Hkv, int D, int page_size, int num_pages,
+    int max_rows, float sm_scale, int dtype, void* out,
+    void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * a4-a7. Accept: vocab pass, p/q acceptance, residual resample, bonus or
+ * fresh draw, proposals and next state.
+ *
+ * [IDLM] "Inference & ISD" / [GN] "Inference & ISD": MASK positions propose
+ * (q), clean positions verify (anchor p), a draft x passes with probability
+ * min(1, p(x)/q(x)).  p and q are softmax(logits / temperature)
+ * (temperature 0 = greedy one-hot argmax).  For a FULL request, draft i
+ * (i = 1..N-1) passes when u_i < min(1, p_i(d_i)/q_i(d_i)), where p_i comes
+ * from clean row i-1 and q_i from the previous step's MASK row that proposed
+ * it; the first failure j ends the scan and its token is drawn from
+ * normalize(max(0, p_j - q_j)) (p_j if that is all zero).  If all N-1 pass,
+ * a bonus token is drawn from p of clean row N-1.  A FRESH request draws one
+ * token from p of its row 0.  Draws are inverse-CDF in vocabulary order with
+ * Philox4x64-10 uniforms (Salmon et al., SC'11): counter (step, c, purpose,
+ * index/4), key (seed, 0), word index%4, u = top 24 bits * 2^-24; purpose 0:
+ * u_i; purpose 1: word 0 bonus/fresh draw, word 1 residual draw; purpose 2:
+ * SAMPLE-mode proposal of MASK row k (index k-1).  Proposals: argmax of each
+ * MASK row (lowest index on ties) or a draw from its q (SAMPLE).
+ *
+ *   logits         [T, V] (dtype)          this step's output rows
+ *   qo_indptr      [C+1] int32
+ *   mode           [C] uint8               IDLM_MODE_FULL / IDLM_MODE_FRESH
+ *   drafts         [C, N-1] int32          read for FULL requests
+ *   draft_q_stats  [C, N-1, 2] float       (m, S) of each draft's proposing
+ *                                          row, as written to next_q_stats by
+ *                                          the previous call
+ *   prev_logits    [prev_rows, V] (dtype)  the previous step's logits
+ *   prev_mask_row0 [C] int32               row of prev_logits that proposed
+ *                                          draft 1 (draft i: row + i - 1), as
+ *                                          written to next_mask_row0 before
+ *   outputs (all [C] unless noted):
+ *   n_accepted     int32    accepted drafts (0 for FRESH)
+ *   out_tokens     [C, N] int32  emitted tokens: accepted drafts, then the
+ *                           resampled / bonus / fresh token; -1 after them
+ *   n_out          int32    n_accepted + 1
+ *   n_commit       int32    rows to commit to the KV cache: 1 + n_accepted
+ *                           (FULL) or 1 (FRESH)
+ *   next_drafts    [C, N-1] int32  proposals if next_mode is FULL, else -1
+ *   next_q_stats   [C, N-1, 2] float (m, S) = (max_v x_v/T,
+ *                           sum_v exp(x_v/T - m)) of each MASK row
+ *   next_mode      uint8    FULL if nothing was rejected, else FRESH
+ *   next_mask_row0 int32    qo_indptr[c] + (number of clean rows)
+ *   row_stats      [T, 2] float or NULL: (m, S) of every row
+ *   dbg            [C, N-1, 4] float or NULL: (u_i, p_i(d_i), q_i(d_i),
+ *                           ratio) per draft of FULL requests
+ * Requirements: V % 8 == 0, 2 <= N <= 16, temperature >= 0.
+ * Device errors: BAD_TOKEN, BAD_LAYOUT (rows of a request disagree with its
+ * mode, qo_indptr leaves [0, T], or a draft's proposing row leaves
+ * [0, prev_rows)).  The call issues one cudaMemsetAsync (workspace counters)
+ * and two kernels.
+ * ---------------------------------------------------------------------- */
+size_t idlm_isd_accept_workspace_size(int C, int T, int N, int V);
+
+idlm_status idlm_isd_accept(
+    const void* logits, int dtype, int V, const int32_t* qo_indptr,
+    const uint8_t* mode, const int32_t* drafts, const float* draft_q_stats,
+    const void* prev_logits, int prev_rows, const int32_t* prev_mask_row0,
+    int C, int T, int N, float temperature, int proposal_mode,
+    uint64_t seed, uint64_t step,
+    int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out, int32_t* n_commit,
+    int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+    int32_t* next_mask_row0, float* row_stats, float* dbg,
+    void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * a8. KV commit / rollback.
+ *
+ * [IDLM] "Serving (SGLang)": paged KV cache.  Rows 0 .. n_commit[c]-1 of
+ * request c (the anchor and its accepted drafts, or a FRESH request's one
+ * clean row) are copied from k_new / v_new to logical slots
+ * L_c .. L_c + n_commit[c] - 1 of the cache.  Rejected drafts and MASK rows
+ * are never written (rollback).  seq_lens_out[c] = L_c + n_commit[c];
+ * releasable_from[c] = ceil(seq_lens_out[c] / page_size): page-table entries
+ * from that index on hold no committed slot and may return to the caller's
+ * pool.  The caller allocates pages for the slots before the call.
+ *
+ *   k_cache, v_cache [num_pages, Hkv, page_size, D]   (dtype) in/out
+ *   page_table      [C, max_pages] int32
+ *   seq_lens_in     [C] int32; seq_lens_out [C] int32 (may be the same buffer)
+ *   k_new, v_new    [T, Hkv, D] (dtype); qo_indptr [C+1] int32 (within [0, T])
+ *   n_commit        [C] int32 (as written by idlm_isd_accept)
+ *   releasable_from [C] int32 or NULL
+ * A request whose commit would touch a page id outside the pool, a slot
+ * beyond its page-table row, or more rows than it has, sets status
+ * (BAD_PAGE, SLOT_OVERFLOW, BAD_LAYOUT) and writes nothing, its length
+ * included.  Requirements: D * element size a multiple of 16 bytes.
+ * ---------------------------------------------------------------------- */
+idlm_status idlm_kv_commit(
+    void* k_cache, void* v_cache, const int32_t* page_table, int max_pages,
+    const int32_t* seq_lens_in, int32_t* seq_lens_out,
+    const void* k_new, const void* v_new, const int32_t* qo_indptr,
+    const int32_t* n_commit, int C, int T, int Hkv, int D, int page_size,
+    int num_pages, int dtype, int32_t* releasable_from, int32_t* status,
+    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDLM_H */

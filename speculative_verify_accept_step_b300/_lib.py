@@ -1,0 +1,160 @@
+"""ctypes binding of libidlm.so: argument marshalling only.
+
+Each function has the name of the C entry point it calls, takes torch tensors
+(device memory) and plain numbers, reads the sizes off the tensors, and passes
+raw pointers and the current CUDA stream to the library.  No arithmetic of the
+ISD step happens here.  A non-OK return raises ``IDLMError``; device-side
+errors land in the caller's ``status`` tensor.
+"""
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libidlm.so")
+
+IDLM_F32 = 0
+IDLM_BF16 = 1
+MODE_FRESH = 0
+MODE_FULL = 1
+PROPOSE_ARGMAX = 0
+PROPOSE_SAMPLE = 1
+
+DEV_STATUS = {0: "ok", 1: "bad page", 2: "bad token", 3: "bad layout", 4: "slot overflow",
+              5: "timeout"}
+
+_lib = None
+
+
+class IDLMError(RuntimeError):
+    pass
+
+
+def lib():
+    """Load libidlm.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise IDLMError(f"{LIB_PATH} is missing: run python -m "
+                            "speculative_verify_accept_step_b300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, u64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64,
+                                 ctypes.c_float, ctypes.c_size_t)
+        L.idlm_version.restype = i32
+        L.idlm_status_string.restype = ctypes.c_char_p
+        L.idlm_status_string.argtypes = [i32]
+        L.idlm_isd_attention_workspace_size.restype = sz
+        L.idlm_isd_attention_workspace_size.argtypes = [i32] * 7
+        L.idlm_isd_attention.restype = i32
+        L.idlm_isd_attention.argtypes = (
+            [vp] * 6 + [i32] + [vp, vp] + [i32] * 8 + [f32, i32, vp, vp, sz, vp, vp])
+        L.idlm_isd_accept_workspace_size.restype = sz
+        L.idlm_isd_accept_workspace_size.argtypes = [i32] * 4
+        L.idlm_isd_accept.restype = i32
+        L.idlm_isd_accept.argtypes = (
+            [vp, i32, i32] + [vp] * 5 + [i32, vp] + [i32, i32, i32, f32, i32, u64, u64]
+            + [vp] * 10
+            + [vp, sz, vp, vp])
+        L.idlm_kv_commit.restype = i32
+        L.idlm_kv_commit.argtypes = ([vp, vp, vp, i32, vp, vp, vp, vp, vp, vp] + [i32] * 7
+                                     + [vp, vp, vp])
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(t):
+    if t.dtype == torch.bfloat16:
+        return IDLM_BF16
+    if t.dtype == torch.float32:
+        return IDLM_F32
+    raise IDLMError(f"unsupported dtype {t.dtype}")
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise IDLMError(f"{what}: {lib().idlm_status_string(rc).decode()} ({rc})")
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise IDLMError("tensors passed to libidlm must be contiguous")
+
+
+def version():
+    return lib().idlm_version()
+
+
+# ------------------------------------------------------------------ attention
+
+def idlm_isd_attention_workspace_size(C, Hq, Hkv, D, page_size, max_rows, dtype):
+    return int(lib().idlm_isd_attention_workspace_size(C, Hq, Hkv, D, page_size, max_rows, dtype))
+
+
+def idlm_isd_attention(q, k_new, v_new, k_cache, v_cache, page_table, seq_lens, qo_indptr,
+                       out, workspace, status, max_rows, sm_scale, stream=None):
+    _contig(q, k_new, v_new, k_cache, v_cache, page_table, seq_lens, qo_indptr, out, workspace)
+    T, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_cache.shape
+    C, max_pages = page_table.shape
+    rc = lib().idlm_isd_attention(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+        max_pages, _ptr(seq_lens), _ptr(qo_indptr), C, T, Hq, Hkv, D, page_size, num_pages,
+        max_rows, float(sm_scale), _dtype(q), _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _check(rc, "idlm_isd_attention")
+
+
+# --------------------------------------------------------------------- accept
+
+def idlm_isd_accept_workspace_size(C, T, N, V):
+    return int(lib().idlm_isd_accept_workspace_size(C, T, N, V))
+
+
+def idlm_isd_accept(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits,
+                    prev_mask_row0, N, temperature, proposal_mode, seed, step,
+                    n_accepted, out_tokens, n_out, n_commit, next_drafts, next_q_stats,
+                    next_mode, next_mask_row0, workspace, status, row_stats=None, dbg=None,
+                    stream=None):
+    _contig(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits, prev_mask_row0,
+            n_accepted, out_tokens, n_out, n_commit, next_drafts, next_q_stats, next_mode,
+            next_mask_row0, workspace, row_stats, dbg)
+    T, V = logits.shape
+    C = mode.shape[0]
+    rc = lib().idlm_isd_accept(
+        _ptr(logits), _dtype(logits), V, _ptr(qo_indptr), _ptr(mode), _ptr(drafts),
+        _ptr(draft_q_stats), _ptr(prev_logits), prev_logits.shape[0], _ptr(prev_mask_row0),
+        C, T, N,
+        float(temperature), int(proposal_mode), int(seed), int(step), _ptr(n_accepted),
+        _ptr(out_tokens), _ptr(n_out), _ptr(n_commit), _ptr(next_drafts), _ptr(next_q_stats),
+        _ptr(next_mode), _ptr(next_mask_row0), _ptr(row_stats), _ptr(dbg), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    _check(rc, "idlm_isd_accept")
+
+
+# --------------------------------------------------------------------- commit
+
+def idlm_kv_commit(k_cache, v_cache, page_table, seq_lens_in, seq_lens_out, k_new, v_new,
+                   qo_indptr, n_commit, status, releasable_from=None, stream=None):
+    _contig(k_cache, v_cache, page_table, seq_lens_in, seq_lens_out, k_new, v_new, qo_indptr,
+            n_commit, releasable_from)
+    num_pages, Hkv, page_size, D = k_cache.shape
+    C, max_pages = page_table.shape
+    rc = lib().idlm_kv_commit(
+        _ptr(k_cache), _ptr(v_cache), _ptr(page_table), max_pages, _ptr(seq_lens_in),
+        _ptr(seq_lens_out), _ptr(k_new), _ptr(v_new), _ptr(qo_indptr), _ptr(n_commit), C,
+        k_new.shape[0], Hkv,
+        D, page_size, num_pages, _dtype(k_cache), _ptr(releasable_from), _ptr(status),
+        _stream(stream))
+    _check(rc, "idlm_kv_commit")

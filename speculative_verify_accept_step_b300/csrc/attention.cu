@@ -1,0 +1,758 @@
+// a2. Paged strict-causal GQA attention of the ISD step rows.
+//
+// Source: "Introspective Diffusion Language Models" (project page), sections
+// "Training" (strict causal masking over all positions) and "Serving
+// (SGLang)" (paged KV cache, paged-only attention kernel).  Row r of request
+// c sits at position L_c + r and attends to committed slots 0..L_c-1 (through
+// the page table) and to this step's own new rows 0..r; query head h reads
+// KV head h / G with G = Hq / Hkv.
+//
+// Fast path (bf16, D = 128, 16-token pages): one work unit is a (request,
+// kv head) pair.  Its G * R query rows (R rows per request, G query heads per
+// kv head; 28 at N = 4) are packed into MT m-tiles of 16 rows, so every KV
+// byte is read from HBM once per unit and reused by all of them.  Work is the
+// list of 16-key blocks of all units (every cached page, plus one block of the
+// step's own new rows per unit); a persistent grid splits that list evenly
+// (balanced split-KV), so long and short contexts load the SMs equally.
+// Units cut by a CTA boundary write partial (max, sum, O) triples to the
+// workspace and the last CTA to finish a unit (atomic arrival count, no
+// waiting) merges them.
+//
+// Per CTA: one producer warp issues TMA tile loads (cp.async.bulk.tensor,
+// 128-byte swizzle) of K and V pages into an 8-stage shared-memory ring
+// guarded by mbarriers; 2*MT consumer warps each own one m-tile and every
+// other block (two parity groups), compute S = Q K^T and O += P V with
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate) and an fp32 online softmax in
+// the log2 domain, and merge the two parity halves at the end of a unit.
+//
+// The general path (fp32, or any other D / page size) is a plain kernel with
+// one warp per (row, head) walking the keys in order.
+#include <algorithm>
+
+#include "common.cuh"
+#include "host_util.h"
+
+namespace idlm {
+namespace attn {
+
+constexpr int D = 128;
+constexpr int PS = 16;
+constexpr int STAGES = 8;
+constexpr int BOX_BYTES = PS * 64 * 2;       // 16 rows x 128 bytes
+constexpr int STAGE_BYTES = 4 * BOX_BYTES;   // K lo/hi half, V lo/hi half
+constexpr int kMaxRequests = 8192;           // prefix array lives in shared memory
+constexpr float kNegInf = -__builtin_inff();
+
+struct Params {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int32_t* qo_indptr;
+  float* ws_o;       // [B][2][MT*16][D]
+  float* ws_ml;      // [B][2][MT*16][2]
+  int32_t* ws_cnt;   // [C*Hkv]
+  int32_t* status;
+  int max_pages, C, T, Hq, Hkv, G, num_pages, max_rows;
+  float scale_log2;  // sm_scale * log2(e)
+};
+
+template <int MT>
+struct Layout {
+  static constexpr int kConsumers = 2 * MT;
+  static constexpr int kThreads = 32 * (1 + kConsumers);
+  static constexpr size_t kStageOff = 0;
+  static constexpr size_t kMergeOOff = kStageOff + size_t(STAGES) * STAGE_BYTES;
+  static constexpr size_t kMergeMLOff = kMergeOOff + size_t(MT) * 16 * D * 4;
+  static constexpr size_t kBarOff = kMergeMLOff + size_t(MT) * 16 * 2 * 4;
+  static constexpr size_t kFlagOff = kBarOff + 2 * STAGES * 8;
+  static constexpr size_t kPrefOff = kFlagOff + 16;
+  static size_t bytes(int C) { return 1024 + kPrefOff + size_t(C + 1) * 4; }
+};
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Position in the global block list -> (request, kv head, block-in-unit).
+struct Cursor {
+  int c, g, k, nb;
+  long long unit_start;
+};
+
+__device__ __forceinline__ Cursor locate(const int* pref, int C, int Hkv, long long j) {
+  // largest c with Hkv * pref[c] <= j
+  int lo = 0, hi = C - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<long long>(Hkv) * pref[mid] <= j) lo = mid; else hi = mid - 1;
+  }
+  Cursor cur;
+  cur.c = lo;
+  cur.nb = pref[lo + 1] - pref[lo];
+  const long long rel = j - static_cast<long long>(Hkv) * pref[lo];
+  cur.g = static_cast<int>(rel / cur.nb);
+  cur.k = static_cast<int>(rel % cur.nb);
+  cur.unit_start = static_cast<long long>(Hkv) * pref[lo] + static_cast<long long>(cur.g) * cur.nb;
+  return cur;
+}
+
+__device__ __forceinline__ void advance(Cursor& cur, const int* pref, int Hkv) {
+  if (++cur.k < cur.nb) return;
+  cur.k = 0;
+  cur.unit_start += cur.nb;
+  if (++cur.g < Hkv) return;
+  cur.g = 0;
+  ++cur.c;
+  cur.nb = pref[cur.c + 1] - pref[cur.c];
+}
+
+__device__ __forceinline__ long long range_lo(long long W, int B, int b) {
+  return W * b / B;
+}
+
+// Index of the CTA whose range holds block x.
+__device__ __forceinline__ int owner_of(long long W, int B, long long x) {
+  return static_cast<int>(((x + 1) * B - 1) / W);
+}
+
+template <int MT>
+__global__ void __launch_bounds__(Layout<MT>::kThreads, MT <= 2 ? 2 : 1)
+paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
+                  const __grid_constant__ CUtensorMap vc_map,
+                  const __grid_constant__ CUtensorMap kn_map,
+                  const __grid_constant__ CUtensorMap vn_map, const Params p) {
+  using LY = Layout<MT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* stages = base + LY::kStageOff;
+  float* merge_o = reinterpret_cast<float*>(base + LY::kMergeOOff);
+  float* merge_ml = reinterpret_cast<float*>(base + LY::kMergeMLOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + LY::kBarOff);
+  uint64_t* empty = full + STAGES;
+  volatile int* flags = reinterpret_cast<volatile int*>(base + LY::kFlagOff);
+  int* pref = reinterpret_cast<int*>(base + LY::kPrefOff);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int C = p.C;
+
+  // ---- blocks per request: ceil(L / 16) cached pages + 1 block of new rows
+  if (tid == 0) {
+    flags[0] = 0;
+    flags[1] = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], MT);
+    }
+    fence_barrier_init();
+  }
+  {
+    const int per = (C + LY::kThreads - 1) / LY::kThreads;
+    const int c0 = min(C, tid * per), c1 = min(C, c0 + per);
+    int sum = 0;
+    for (int c = c0; c < c1; ++c) {
+      int L = p.seq_lens[c];
+      const int rows = p.qo_indptr[c + 1] - p.qo_indptr[c];
+      if (L < 0 || rows < 0 || rows > p.max_rows || p.qo_indptr[c] < 0 ||
+          p.qo_indptr[c + 1] > p.T)
+        set_status(p.status, IDLM_DEV_BAD_LAYOUT);
+      if (L > p.max_pages * PS) set_status(p.status, IDLM_DEV_SLOT_OVERFLOW);
+      L = min(max(L, 0), p.max_pages * PS);
+      pref[c + 1] = (L + PS - 1) / PS + 1;   // temporarily the count
+      sum += pref[c + 1];
+    }
+    __syncthreads();
+    // serial scan of the per-thread sums by thread 0, then local fix-up
+    __shared__ int part[LY::kThreads + 1];
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+      int acc = 0;
+      for (int t = 0; t < LY::kThreads; ++t) {
+        const int v = part[t];
+        part[t] = acc;
+        acc += v;
+      }
+      pref[0] = 0;
+    }
+    __syncthreads();
+    int acc = part[tid];
+    for (int c = c0; c < c1; ++c) {
+      acc += pref[c + 1];
+      pref[c + 1] = acc;
+    }
+  }
+  fence_proxy_async();
+  __syncthreads();
+
+  const long long W = static_cast<long long>(p.Hkv) * pref[C];
+  const int B = gridDim.x;
+  const long long lo = range_lo(W, B, blockIdx.x);
+  const long long hi = range_lo(W, B, blockIdx.x + 1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && lo < hi) {
+      prefetch_tensormap(&kc_map);
+      prefetch_tensormap(&vc_map);
+      prefetch_tensormap(&kn_map);
+      prefetch_tensormap(&vn_map);
+      Cursor cur = locate(pref, C, p.Hkv, lo);
+      int issued = 0;
+      for (long long j = lo; j < hi; ++j) {
+        const int s = issued % STAGES;
+        const uint32_t ph = (issued / STAGES) & 1;
+        if (!mbar_wait_bounded(&empty[s], ph ^ 1, flags, p.status)) break;
+        uint8_t* dst = stages + s * STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+        const int nbc = cur.nb - 1;
+        if (cur.k < nbc) {
+          const int page = p.page_table[static_cast<size_t>(cur.c) * p.max_pages + cur.k];
+          int y;
+          if (page < 0 || page >= p.num_pages) {
+            set_status(p.status, IDLM_DEV_BAD_PAGE);
+            y = -2 * PS;   // wholly outside the tensor: the copy fills zeros
+          } else {
+            y = (page * p.Hkv + cur.g) * PS;
+          }
+          tma_load_2d(dst, &kc_map, &full[s], 0, y);
+          tma_load_2d(dst + BOX_BYTES, &kc_map, &full[s], 64, y);
+          tma_load_2d(dst + 2 * BOX_BYTES, &vc_map, &full[s], 0, y);
+          tma_load_2d(dst + 3 * BOX_BYTES, &vc_map, &full[s], 64, y);
+        } else {
+          const int t0 = p.qo_indptr[cur.c];
+          tma_load_3d(dst, &kn_map, &full[s], 0, cur.g, t0);
+          tma_load_3d(dst + BOX_BYTES, &kn_map, &full[s], 64, cur.g, t0);
+          tma_load_3d(dst + 2 * BOX_BYTES, &vn_map, &full[s], 0, cur.g, t0);
+          tma_load_3d(dst + 3 * BOX_BYTES, &vn_map, &full[s], 64, cur.g, t0);
+        }
+        ++issued;
+        advance(cur, pref, p.Hkv);
+      }
+      // every issued copy must land before the CTA may exit
+      for (int i = max(0, issued - STAGES); i < issued; ++i)
+        mbar_wait_bounded(&full[i % STAGES], (i / STAGES) & 1, nullptr, p.status);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int cw = warp - 1;
+  const int mt = cw % MT;
+  const int par = cw / MT;
+  const int qr = lane >> 2;       // fragment row within the m-tile (and +8)
+  const int qc = (lane & 3) * 2;  // fragment column pair
+  const int G = p.G;
+  const int row_a = 16 * mt + qr, row_b = row_a + 8;   // packed rows m
+  const int r_a = row_a / G, hl_a = row_a % G;
+  const int r_b = row_b / G, hl_b = row_b % G;
+  const int key_ld = (lane & 7) + ((lane >> 4) << 3);
+  const int kch_off = (lane >> 3) & 1;
+  const int vkey = lane & 15;
+  const int vch_off = lane >> 4;
+
+  Cursor cur = locate(pref, C, p.Hkv, lo < hi ? lo : 0);
+  long long j = lo;
+  int i = 0;
+  while (j < hi) {
+    const long long unit_end = cur.unit_start + cur.nb;
+    const long long seg_start = j;
+    const long long seg_end = min(hi, unit_end);
+    const bool whole = (seg_start == cur.unit_start) && (seg_end == unit_end);
+    const int c = cur.c, g = cur.g;
+    const int L = min(max(p.seq_lens[c], 0), p.max_pages * PS);
+    const int t0 = min(max(p.qo_indptr[c], 0), p.T);
+    const int R = min(min(max(p.qo_indptr[c + 1] - t0, 0), p.max_rows), p.T - t0);
+    const bool va = r_a < R, vb = r_b < R;
+    const int nbc = cur.nb - 1;
+
+    // Q fragments of this m-tile (rows past R are zero)
+    uint32_t qa[8][4];
+    {
+      const uint32_t* qa_ptr = reinterpret_cast<const uint32_t*>(
+          p.q + (static_cast<size_t>(t0 + r_a) * p.Hq + g * G + hl_a) * D);
+      const uint32_t* qb_ptr = reinterpret_cast<const uint32_t*>(
+          p.q + (static_cast<size_t>(t0 + r_b) * p.Hq + g * G + hl_b) * D);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int col = (16 * ks + qc) >> 1;
+        qa[ks][0] = va ? __ldg(qa_ptr + col) : 0u;
+        qa[ks][1] = vb ? __ldg(qb_ptr + col) : 0u;
+        qa[ks][2] = va ? __ldg(qa_ptr + col + 4) : 0u;
+        qa[ks][3] = vb ? __ldg(qb_ptr + col + 4) : 0u;
+      }
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
+
+    for (; j < seg_end; ++j, ++i, advance(cur, pref, p.Hkv)) {
+      if ((i & 1) != par) continue;
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      const bool ok = mbar_wait_bounded(&full[s], ph, flags, p.status);
+      if (ok) {
+        const uint32_t kbase = smem_u32(stages + s * STAGE_BYTES);
+        const uint32_t vbase = kbase + 2 * BOX_BYTES;
+        float sc[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const int ch = 2 * ks + kch_off;
+          const uint32_t addr = kbase + (ch >> 3) * BOX_BYTES + key_ld * 128 +
+                                (((ch & 7) ^ (key_ld & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_bf16_16816(sc[0], qa[ks], b0, b1);
+          mma_bf16_16816(sc[1], qa[ks], b2, b3);
+        }
+        // scale and mask: column key = 8n + qc + e
+        const int k = cur.k;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = 8 * n + qc + e;
+            bool ka, kb;
+            if (k < nbc) {
+              ka = kb = (k * PS + key) < L;
+            } else {
+              ka = key <= r_a;
+              kb = key <= r_b;
+            }
+            sc[n][e] = ka ? sc[n][e] * p.scale_log2 : kNegInf;
+            sc[n][2 + e] = kb ? sc[n][2 + e] * p.scale_log2 : kNegInf;
+          }
+        }
+        float mx_a = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        float mx_b = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+        const float base_a = mn_a == kNegInf ? 0.f : mn_a;
+        const float base_b = mn_b == kNegInf ? 0.f : mn_b;
+        const float corr_a = fast_exp2(m_a - base_a), corr_b = fast_exp2(m_b - base_b);
+        m_a = mn_a;
+        m_b = mn_b;
+        float pr[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          pr[n][0] = fast_exp2(sc[n][0] - base_a);
+          pr[n][1] = fast_exp2(sc[n][1] - base_a);
+          pr[n][2] = fast_exp2(sc[n][2] - base_b);
+          pr[n][3] = fast_exp2(sc[n][3] - base_b);
+        }
+        l_a = l_a * corr_a + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
+        l_b = l_b * corr_b + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          o[n][0] *= corr_a;
+          o[n][1] *= corr_a;
+          o[n][2] *= corr_b;
+          o[n][3] *= corr_b;
+        }
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+        pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+        pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+        pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {
+          const int ch = 2 * dp + vch_off;
+          const uint32_t addr = vbase + (ch >> 3) * BOX_BYTES + vkey * 128 +
+                                (((ch & 7) ^ (vkey & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(addr, b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * dp], pa, b0, b1);
+          mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ---- end of this unit's segment: merge the two parity halves
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    float* mo = merge_o + mt * 16 * D;
+    float* mml = merge_ml + mt * 32;
+    if (par == 1) {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        *reinterpret_cast<float2*>(mo + qr * D + 8 * n + qc) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(mo + (qr + 8) * D + 8 * n + qc) = make_float2(o[n][2], o[n][3]);
+      }
+      if ((lane & 3) == 0) {
+        mml[2 * qr] = m_a;
+        mml[2 * qr + 1] = l_a;
+        mml[2 * (qr + 8)] = m_b;
+        mml[2 * (qr + 8) + 1] = l_b;
+      }
+    }
+    named_bar(1 + mt, 64);
+    if (par == 0) {
+      const float m2a = mml[2 * qr], l2a = mml[2 * qr + 1];
+      const float m2b = mml[2 * (qr + 8)], l2b = mml[2 * (qr + 8) + 1];
+      const float Ma = fmaxf(m_a, m2a), Mb = fmaxf(m_b, m2b);
+      const float ba = Ma == kNegInf ? 0.f : Ma, bb = Mb == kNegInf ? 0.f : Mb;
+      const float fa1 = fast_exp2(m_a - ba), fa2 = fast_exp2(m2a - ba);
+      const float fb1 = fast_exp2(m_b - bb), fb2 = fast_exp2(m2b - bb);
+      l_a = l_a * fa1 + l2a * fa2;
+      l_b = l_b * fb1 + l2b * fb2;
+      m_a = Ma;
+      m_b = Mb;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        const float2 xa = *reinterpret_cast<const float2*>(mo + qr * D + 8 * n + qc);
+        const float2 xb = *reinterpret_cast<const float2*>(mo + (qr + 8) * D + 8 * n + qc);
+        o[n][0] = o[n][0] * fa1 + xa.x * fa2;
+        o[n][1] = o[n][1] * fa1 + xa.y * fa2;
+        o[n][2] = o[n][2] * fb1 + xb.x * fb2;
+        o[n][3] = o[n][3] * fb1 + xb.y * fb2;
+      }
+    }
+    named_bar(1 + mt, 64);
+
+    if (par == 0) {
+      const int h_a = g * G + hl_a, h_b = g * G + hl_b;
+      uint32_t* out_a = reinterpret_cast<uint32_t*>(p.out + (static_cast<size_t>(t0 + r_a) * p.Hq + h_a) * D);
+      uint32_t* out_b = reinterpret_cast<uint32_t*>(p.out + (static_cast<size_t>(t0 + r_b) * p.Hq + h_b) * D);
+      if (whole) {
+        const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          if (va) out_a[(8 * n + qc) >> 1] = pack_bf16x2(o[n][0] * ia, o[n][1] * ia);
+          if (vb) out_b[(8 * n + qc) >> 1] = pack_bf16x2(o[n][2] * ib, o[n][3] * ib);
+        }
+      } else {
+        // partial: slot 0 if this segment opened the CTA's range, else slot 1
+        const int slot = (seg_start == lo) ? 0 : 1;
+        const size_t sbase = (static_cast<size_t>(blockIdx.x) * 2 + slot) * (MT * 16);
+        float* wo = p.ws_o + sbase * D;
+        float* wml = p.ws_ml + sbase * 2;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          *reinterpret_cast<float2*>(wo + row_a * D + 8 * n + qc) = make_float2(o[n][0], o[n][1]);
+          *reinterpret_cast<float2*>(wo + row_b * D + 8 * n + qc) = make_float2(o[n][2], o[n][3]);
+        }
+        if ((lane & 3) == 0) {
+          wml[2 * row_a] = m_a;
+          wml[2 * row_a + 1] = l_a;
+          wml[2 * row_b] = m_b;
+          wml[2 * row_b + 1] = l_b;
+        }
+        __threadfence();
+        named_bar(1 + MT, 32 * MT);
+        const int u = c * p.Hkv + g;
+        const long long ustart = unit_end - (nbc + 1);
+        const int bf = owner_of(W, B, ustart);
+        const int bl = owner_of(W, B, unit_end - 1);
+        if (mt == 0 && lane == 0) {
+          // CTAs with an empty range (more CTAs than blocks) hold no part
+          int parts = 0;
+          for (int b = bf; b <= bl; ++b) parts += range_lo(W, B, b) < range_lo(W, B, b + 1);
+          const int old = atomicAdd(&p.ws_cnt[u], 1);
+          const int last = (old == parts - 1);
+          if (last) p.ws_cnt[u] = 0;
+          flags[1] = last;
+        }
+        named_bar(1 + MT, 32 * MT);
+        const bool last = flags[1] != 0;
+        if (last) {
+          __threadfence();
+          float Ma = kNegInf, Mb = kNegInf;
+          for (int b = bf; b <= bl; ++b) {
+            if (range_lo(W, B, b) >= range_lo(W, B, b + 1)) continue;
+            const int sl = (b == bf && ustart > range_lo(W, B, b)) ? 1 : 0;
+            const size_t pb = (static_cast<size_t>(b) * 2 + sl) * (MT * 16);
+            Ma = fmaxf(Ma, __ldcg(p.ws_ml + (pb + row_a) * 2));
+            Mb = fmaxf(Mb, __ldcg(p.ws_ml + (pb + row_b) * 2));
+          }
+          const float ba = Ma == kNegInf ? 0.f : Ma, bb = Mb == kNegInf ? 0.f : Mb;
+          float La = 0.f, Lb = 0.f;
+#pragma unroll
+          for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+          for (int b = bf; b <= bl; ++b) {
+            if (range_lo(W, B, b) >= range_lo(W, B, b + 1)) continue;
+            const int sl = (b == bf && ustart > range_lo(W, B, b)) ? 1 : 0;
+            const size_t pb = (static_cast<size_t>(b) * 2 + sl) * (MT * 16);
+            const float fa = fast_exp2(__ldcg(p.ws_ml + (pb + row_a) * 2) - ba);
+            const float fb = fast_exp2(__ldcg(p.ws_ml + (pb + row_b) * 2) - bb);
+            La += fa * __ldcg(p.ws_ml + (pb + row_a) * 2 + 1);
+            Lb += fb * __ldcg(p.ws_ml + (pb + row_b) * 2 + 1);
+            const float* po = p.ws_o + pb * D;
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+              const float2 xa = __ldcg(reinterpret_cast<const float2*>(po + row_a * D + 8 * n + qc));
+              const float2 xb = __ldcg(reinterpret_cast<const float2*>(po + row_b * D + 8 * n + qc));
+              o[n][0] += fa * xa.x;
+              o[n][1] += fa * xa.y;
+              o[n][2] += fb * xb.x;
+              o[n][3] += fb * xb.y;
+            }
+          }
+          const float ia = La > 0.f ? 1.f / La : 0.f, ib = Lb > 0.f ? 1.f / Lb : 0.f;
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            if (va) out_a[(8 * n + qc) >> 1] = pack_bf16x2(o[n][0] * ia, o[n][1] * ia);
+            if (vb) out_b[(8 * n + qc) >> 1] = pack_bf16x2(o[n][2] * ib, o[n][3] * ib);
+          }
+        }
+        named_bar(1 + MT, 32 * MT);
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------- general path
+// One warp per (row, query head); lanes split D; keys visited in order with
+// an online softmax in fp32.  Any page size, D a multiple of 32 up to 256.
+template <typename T>
+__device__ __forceinline__ float ld_f(const T* p);
+template <>
+__device__ __forceinline__ float ld_f<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+template <typename T>
+__device__ __forceinline__ void st_f(T* p, float v);
+template <>
+__device__ __forceinline__ void st_f<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void st_f<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128)
+simple_attn_kernel(const T* q, const T* k_new, const T* v_new, const T* k_cache,
+                   const T* v_cache, const int32_t* page_table, int max_pages,
+                   const int32_t* seq_lens, const int32_t* qo_indptr, int C, int T_rows,
+                   int Hq, int Hkv, int D_, int page_size, int num_pages, int max_rows,
+                   float scale, T* out, int32_t* status) {
+  const int t = blockIdx.x;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T_rows || h >= Hq) return;
+  // request of row t
+  int lo = 0, hi = C - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (qo_indptr[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int c = lo;
+  const int t0 = qo_indptr[c];
+  const int r = t - t0;
+  const int rows = qo_indptr[c + 1] - t0;
+  if (rows > max_rows || seq_lens[c] < 0) set_status(status, IDLM_DEV_BAD_LAYOUT);
+  const int L = max(seq_lens[c], 0);
+  const int g = h / (Hq / Hkv);
+  const int per = D_ / 32;  // elements per lane
+  float qv[8], acc[8];
+  for (int e = 0; e < per; ++e) {
+    qv[e] = ld_f(q + (static_cast<size_t>(t) * Hq + h) * D_ + lane * per + e);
+    acc[e] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  const int total = L + r + 1;
+  for (int s = 0; s < total; ++s) {
+    const T* kp;
+    const T* vp;
+    if (s < L) {
+      const int pi = s / page_size;
+      int page = pi < max_pages ? page_table[static_cast<size_t>(c) * max_pages + pi] : -1;
+      if (page < 0 || page >= num_pages) {
+        set_status(status, IDLM_DEV_BAD_PAGE);
+        continue;
+      }
+      const size_t off = ((static_cast<size_t>(page) * Hkv + g) * page_size + s % page_size) * D_;
+      kp = k_cache + off;
+      vp = v_cache + off;
+    } else {
+      const size_t off = (static_cast<size_t>(t0 + (s - L)) * Hkv + g) * D_;
+      kp = k_new + off;
+      vp = v_new + off;
+    }
+    float dot = 0.f;
+    for (int e = 0; e < per; ++e) dot += qv[e] * ld_f(kp + lane * per + e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    const float sc = dot * scale;
+    const float mn = fmaxf(m, sc);
+    const float corr = expf(m - mn);
+    const float pr = expf(sc - mn);
+    l = l * corr + pr;
+    for (int e = 0; e < per; ++e) acc[e] = acc[e] * corr + pr * ld_f(vp + lane * per + e);
+    m = mn;
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  for (int e = 0; e < per; ++e)
+    st_f(out + (static_cast<size_t>(t) * Hq + h) * D_ + lane * per + e, acc[e] * inv);
+}
+
+template <int MT>
+size_t workspace_for(int C, int Hkv, int B) {
+  Carver cv(nullptr);
+  cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * D);
+  cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * 2);
+  cv.take<int32_t>(static_cast<size_t>(C) * Hkv);
+  return cv.used;
+}
+
+template <int MT>
+int grid_for(const DeviceInfo& dev, int C) {
+  const size_t smem = Layout<MT>::bytes(C);
+  int per_sm = 0;
+  if (cudaFuncSetAttribute(paged_attn_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, paged_attn_kernel<MT>,
+                                                    Layout<MT>::kThreads, smem) != cudaSuccess)
+    return 0;
+  return dev.sm_count * std::max(per_sm, 1);
+}
+
+inline int mtiles_for(int G, int max_rows) { return (G * max_rows + 15) / 16; }
+
+bool use_fast_path(int dtype, int D_, int page_size, int G, int max_rows, int C) {
+  const int mtl = mtiles_for(G, max_rows);
+  return dtype == IDLM_BF16 && D_ == D && page_size == PS && mtl >= 1 && mtl <= 4 &&
+         C <= kMaxRequests;
+}
+
+template <int MT>
+idlm_status launch_fast(const DeviceInfo& dev, const void* q, const void* k_new,
+                        const void* v_new, const void* k_cache, const void* v_cache,
+                        const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                        const int32_t* qo_indptr, int C, int T, int Hq, int Hkv,
+                        int num_pages, int max_rows, float sm_scale, void* out,
+                        void* workspace, size_t ws_bytes, int32_t* status,
+                        cudaStream_t stream) {
+  const int B = grid_for<MT>(dev, C);
+  if (B <= 0) return IDLM_ERR_CUDA;
+  if (ws_bytes < workspace_for<MT>(C, Hkv, B) || !workspace) return IDLM_ERR_WORKSPACE;
+  Carver cv(workspace);
+  Params p;
+  p.ws_o = cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * D);
+  p.ws_ml = cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * 2);
+  p.ws_cnt = cv.take<int32_t>(static_cast<size_t>(C) * Hkv);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.qo_indptr = qo_indptr;
+  p.status = status;
+  p.max_pages = max_pages;
+  p.C = C;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.num_pages = num_pages;
+  p.max_rows = max_rows;
+  p.scale_log2 = sm_scale * kLog2e;
+
+  CUtensorMap kc, vc, kn, vn;
+  const uint64_t cdims[2] = {static_cast<uint64_t>(D),
+                             static_cast<uint64_t>(num_pages) * Hkv * PS};
+  const uint64_t cstr[1] = {D * 2};
+  const uint32_t cbox[2] = {64, PS};
+  const uint64_t ndims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
+                             static_cast<uint64_t>(T)};
+  const uint64_t nstr[2] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2};
+  const uint32_t nbox[3] = {64, 1, PS};
+  if (!encode_bf16_map(&kc, const_cast<void*>(k_cache), 2, cdims, cstr, cbox) ||
+      !encode_bf16_map(&vc, const_cast<void*>(v_cache), 2, cdims, cstr, cbox) ||
+      !encode_bf16_map(&kn, const_cast<void*>(k_new), 3, ndims, nstr, nbox) ||
+      !encode_bf16_map(&vn, const_cast<void*>(v_new), 3, ndims, nstr, nbox))
+    return IDLM_ERR_CUDA;
+
+  cudaError_t e = cudaMemsetAsync(p.ws_cnt, 0, static_cast<size_t>(C) * Hkv * sizeof(int32_t), stream);
+  if (e != cudaSuccess) return IDLM_ERR_CUDA;
+  paged_attn_kernel<MT><<<B, Layout<MT>::kThreads, Layout<MT>::bytes(C), stream>>>(kc, vc, kn, vn, p);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace attn
+}  // namespace idlm
+
+using namespace idlm;
+
+extern "C" size_t idlm_isd_attention_workspace_size(int C, int Hq, int Hkv, int D_,
+                                                    int page_size, int max_rows, int dtype) {
+  if (C <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv) return 0;
+  const int G = Hq / Hkv;
+  if (!attn::use_fast_path(dtype, D_, page_size, G, max_rows, C)) return 256;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return 0;
+  switch (attn::mtiles_for(G, max_rows)) {
+    case 1: return attn::workspace_for<1>(C, Hkv, attn::grid_for<1>(dev, C));
+    case 2: return attn::workspace_for<2>(C, Hkv, attn::grid_for<2>(dev, C));
+    case 3: return attn::workspace_for<3>(C, Hkv, attn::grid_for<3>(dev, C));
+    default: return attn::workspace_for<4>(C, Hkv, attn::grid_for<4>(dev, C));
+  }
+}
+
+extern "C" idlm_status idlm_isd_attention(
+    const void* q, const void* k_new, const void* v_new, const void* k_cache,
+    const void* v_cache, const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+    const int32_t* qo_indptr, int C, int T, int Hq, int Hkv, int D_, int page_size,
+    int num_pages, int max_rows, float sm_scale, int dtype, void* out, void* workspace,
+    size_t workspace_bytes, int32_t* status, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !page_table || !seq_lens ||
+      !qo_indptr || !out || !status)
+    return IDLM_ERR_INVALID_ARG;
+  if (C <= 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D_ <= 0 || page_size <= 0 ||
+      num_pages <= 0 || max_pages <= 0 || max_rows <= 0 || !(sm_scale > 0.f))
+    return IDLM_ERR_INVALID_ARG;
+  if (dtype != IDLM_BF16 && dtype != IDLM_F32) return IDLM_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (attn::use_fast_path(dtype, D_, page_size, G, max_rows, C)) {
+    DeviceInfo dev;
+    if (!current_device_info(&dev)) return IDLM_ERR_CUDA;
+    // TMA needs 16-byte aligned bases
+    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+         reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+      return IDLM_ERR_INVALID_ARG;
+#define IDLM_FAST(MT)                                                                          \
+  return attn::launch_fast<MT>(dev, q, k_new, v_new, k_cache, v_cache, page_table, max_pages, \
+                               seq_lens, qo_indptr, C, T, Hq, Hkv, num_pages, max_rows,       \
+                               sm_scale, out, workspace, workspace_bytes, status, stream)
+    switch (attn::mtiles_for(G, max_rows)) {
+      case 1: IDLM_FAST(1);
+      case 2: IDLM_FAST(2);
+      case 3: IDLM_FAST(3);
+      default: IDLM_FAST(4);
+    }
+#undef IDLM_FAST
+  }
+  if (D_ % 32 || D_ > 256) return IDLM_ERR_UNSUPPORTED;
+  dim3 grid(T, (Hq + 3) / 4);
+  if (dtype == IDLM_BF16) {
+    attn::simple_attn_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
+        static_cast<const __nv_bfloat16*>(v_new), static_cast<const __nv_bfloat16*>(k_cache),
+        static_cast<const __nv_bfloat16*>(v_cache), page_table, max_pages, seq_lens, qo_indptr,
+        C, T, Hq, Hkv, D_, page_size, num_pages, max_rows, sm_scale,
+        static_cast<__nv_bfloat16*>(out), status);
+  } else {
+    attn::simple_attn_kernel<float><<<grid, 128, 0, stream>>>(
+        static_cast<const float*>(q), static_cast<const float*>(k_new),
+        static_cast<const float*>(v_new), static_cast<const float*>(k_cache),
+        static_cast<const float*>(v_cache), page_table, max_pages, seq_lens, qo_indptr, C, T,
+        Hq, Hkv, D_, page_size, num_pages, max_rows, sm_scale, static_cast<float*>(out),
+        status);
+  }
+  return cuda_status(cudaGetLastError());
+}

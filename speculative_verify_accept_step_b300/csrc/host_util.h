@@ -1,0 +1,51 @@
+// Host-side helpers shared by the entry points: device properties, TMA tensor
+// map encoding through the driver entry point (no link against libcuda), and
+// workspace carving.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/idlm.h"
+
+namespace idlm {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int max_smem_optin = 0;
+};
+
+// Properties of the current device (cached per device ordinal).
+bool current_device_info(DeviceInfo* out);
+
+// cuTensorMapEncodeTiled, resolved once from the driver.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// Encode a tiled bf16 tensor map with 128-byte swizzle.
+// dims/strides are innermost first; strides (bytes) exclude dimension 0.
+bool encode_bf16_map(CUtensorMap* map, void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Carve consecutive 256-byte aligned regions out of a workspace.
+struct Carver {
+  uint8_t* base;
+  size_t used = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <class T>
+  T* take(size_t count) {
+    used = align_up(used, 256);
+    T* p = base ? reinterpret_cast<T*>(base + used) : nullptr;
+    used += count * sizeof(T);
+    return p;
+  }
+};
+
+inline idlm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? IDLM_OK : IDLM_ERR_CUDA; }
+
+}  // namespace idlm
