@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--workload", default="isd_c64_n4_ctx4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--profile-run", action="store_true",
+                    help="few launches for a profiler: no clock sampling, e2e or CPU leg")
     return ap.parse_args()
 
 
@@ -263,12 +265,13 @@ def run_ours(args):
         st.commit(wo)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
-    clocks.start()
+    if not args.profile_run:
+        clocks.start()
     # keep the GPU loaded for ~0.6 s while the sampler starts, so its readings
     # before the timed region are taken under the same load
     t_load = time.time()
     i = 0
-    while time.time() - t_load < 0.6:
+    while time.time() - t_load < 0.6 and not args.profile_run:
         for _ in range(50):
             st.attention()
             st.accept(wo, 20_000_000 + i)
@@ -309,9 +312,9 @@ def run_ours(args):
     acc_gbs = c_bytes / (acc_ms * 1e-3) / 1e9
     both_gbs = (a_bytes + c_bytes) / ((att_ms + acc_ms) * 1e-3) / 1e9
 
-    e2e = run_e2e(st, args.e2e_steps, ws)
+    e2e = None if args.profile_run else run_e2e(st, args.e2e_steps, ws)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.profile_run:
         cpu = cpu_baseline(w, st.host)
     if rank != 0:
         return
