@@ -195,6 +195,38 @@ idlm_status idlm_isd_accept(
     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free accept.  The pages have no counterpart: this entry point
+ * exists for callers that cannot allocate device memory -- a plugin whose
+ * host owns all GPU memory and offers no scratch, or a decode loop held to a
+ * fixed memory budget that may not call the allocator while it runs.
+ *
+ * Same arguments and results as idlm_isd_accept without the workspace pair.
+ * The scratch is one 4 MiB array compiled into the library (a static
+ * __device__ array), which every GPU that loads the library keeps until the
+ * process exits.  The call allocates nothing and frees nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Returns IDLM_ERR_WORKSPACE, launching nothing, when the call needs more
+ *     than 4 MiB, i.e. when idlm_isd_accept_workspace_size(C, T, N, V)
+ *     exceeds 4194304 bytes.
+ *   - Every call uses the same array and it keeps the last call's contents;
+ *     each call clears the counters it relies on before its kernels run.
+ *     Calls that can overlap on the GPU (two streams, two host threads) race
+ *     on the array and corrupt each other's results: serialise them.
+ * ---------------------------------------------------------------------- */
+idlm_status idlm_isd_accept_noalloc(
+    const void* logits, int dtype, int V, const int32_t* qo_indptr,
+    const uint8_t* mode, const int32_t* drafts, const float* draft_q_stats,
+    const void* prev_logits, int prev_rows, const int32_t* prev_mask_row0,
+    int C, int T, int N, float temperature, int proposal_mode,
+    uint64_t seed, uint64_t step,
+    int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out, int32_t* n_commit,
+    int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+    int32_t* next_mask_row0, float* row_stats, float* dbg,
+    int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * a8. KV commit / rollback.
  *
  * [IDLM] "Serving (SGLang)": paged KV cache.  Rows 0 .. n_commit[c]-1 of

@@ -56,6 +56,10 @@ def lib():
             [vp, i32, i32] + [vp] * 5 + [i32, vp] + [i32, i32, i32, f32, i32, u64, u64]
             + [vp] * 10
             + [vp, sz, vp, vp])
+        L.idlm_isd_accept_noalloc.restype = i32
+        L.idlm_isd_accept_noalloc.argtypes = (
+            [vp, i32, i32] + [vp] * 5 + [i32, vp] + [i32, i32, i32, f32, i32, u64, u64]
+            + [vp] * 10 + [vp, vp])
         L.idlm_kv_commit.restype = i32
         L.idlm_kv_commit.argtypes = ([vp, vp, vp, i32, vp, vp, vp, vp, vp, vp] + [i32] * 7
                                      + [vp, vp, vp])
@@ -141,6 +145,29 @@ def idlm_isd_accept(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits,
         _ptr(next_mode), _ptr(next_mask_row0), _ptr(row_stats), _ptr(dbg), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
     _check(rc, "idlm_isd_accept")
+
+
+def idlm_isd_accept_noalloc(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits,
+                            prev_mask_row0, N, temperature, proposal_mode, seed, step,
+                            n_accepted, out_tokens, n_out, n_commit, next_drafts, next_q_stats,
+                            next_mode, next_mask_row0, status, row_stats=None, dbg=None,
+                            stream=None):
+    """idlm_isd_accept without a workspace: the library's fixed 4 MiB scratch
+    array is used instead, so the call allocates nothing.  Calls that may
+    overlap on the GPU share that array and must be serialised."""
+    _contig(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits, prev_mask_row0,
+            n_accepted, out_tokens, n_out, n_commit, next_drafts, next_q_stats, next_mode,
+            next_mask_row0, row_stats, dbg)
+    T, V = logits.shape
+    C = mode.shape[0]
+    rc = lib().idlm_isd_accept_noalloc(
+        _ptr(logits), _dtype(logits), V, _ptr(qo_indptr), _ptr(mode), _ptr(drafts),
+        _ptr(draft_q_stats), _ptr(prev_logits), prev_logits.shape[0], _ptr(prev_mask_row0),
+        C, T, N, float(temperature), int(proposal_mode), int(seed), int(step),
+        _ptr(n_accepted), _ptr(out_tokens), _ptr(n_out), _ptr(n_commit), _ptr(next_drafts),
+        _ptr(next_q_stats), _ptr(next_mode), _ptr(next_mask_row0), _ptr(row_stats), _ptr(dbg),
+        _ptr(status), _stream(stream))
+    _check(rc, "idlm_isd_accept_noalloc")
 
 
 # --------------------------------------------------------------------- commit

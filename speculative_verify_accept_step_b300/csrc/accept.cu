@@ -25,6 +25,7 @@
 // step) and q_j (the previous step's MASK row); the last CTA draws the token
 // by inverse CDF the same way.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "host_util.h"
@@ -711,4 +712,60 @@ extern "C" idlm_status idlm_isd_accept(
     acc::residual_kernel<float><<<C * CH, acc::kThreads, 0, stream>>>(p);
   }
   return cuda_status(cudaGetLastError());
+}
+
+// ------------------------------------------------------- allocation-free entry
+//
+// Some callers cannot allocate device memory at all: a plugin whose host
+// process owns every byte of the GPU and hands out no scratch, or a decode
+// loop that runs under a fixed memory budget and must not call the allocator
+// once it is running.  For them, idlm_isd_accept_noalloc runs the same accept
+// step with its scratch in a fixed array compiled into this library.
+
+namespace idlm {
+namespace acc {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;   // 4 MiB, per GPU
+static __device__ __align__(256) uint8_t g_accept_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
+}  // namespace
+
+// Device address of g_accept_scratch on the current device, looked up once
+// per device.  In host code the array's name is only a host-side handle; the
+// kernels need the address cudaGetSymbolAddress returns.
+void* static_scratch() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace acc
+}  // namespace idlm
+
+extern "C" idlm_status idlm_isd_accept_noalloc(
+    const void* logits, int dtype, int V, const int32_t* qo_indptr, const uint8_t* mode,
+    const int32_t* drafts, const float* draft_q_stats, const void* prev_logits, int prev_rows,
+    const int32_t* prev_mask_row0, int C, int T, int N, float temperature, int proposal_mode,
+    uint64_t seed, uint64_t step, int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out,
+    int32_t* n_commit, int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+    int32_t* next_mask_row0, float* row_stats, float* dbg, int32_t* status, void* stream) {
+  if (C <= 0 || T <= 0 || V <= 0) return IDLM_ERR_INVALID_ARG;
+  if (acc::workspace_bytes(C, T, V, nullptr, nullptr) > acc::kStaticScratchBytes)
+    return IDLM_ERR_WORKSPACE;
+  void* scratch = acc::static_scratch();
+  if (!scratch) return IDLM_ERR_CUDA;
+  return idlm_isd_accept(logits, dtype, V, qo_indptr, mode, drafts, draft_q_stats, prev_logits,
+                         prev_rows, prev_mask_row0, C, T, N, temperature, proposal_mode, seed,
+                         step, n_accepted, out_tokens, n_out, n_commit, next_drafts,
+                         next_q_stats, next_mode, next_mask_row0, row_stats, dbg, scratch,
+                         acc::kStaticScratchBytes, status, stream);
 }
