@@ -178,8 +178,11 @@ idlm_status idlm_isd_attention(
  * Requirements: V % 8 == 0, 2 <= N <= 16, temperature >= 0.
  * Device errors: BAD_TOKEN, BAD_LAYOUT (rows of a request disagree with its
  * mode, qo_indptr leaves [0, T], or a draft's proposing row leaves
- * [0, prev_rows)).  The call issues one cudaMemsetAsync (workspace counters)
- * and two kernels.
+ * [0, prev_rows)).  The call launches three kernels and nothing else: a
+ * streaming pass over the logits, a per-request decision kernel and a
+ * residual kernel, the last two as programmatic dependents of the kernel
+ * before them (plain stream order where the stream does not take that
+ * attribute).  Workspace contents need no initialisation.
  * ---------------------------------------------------------------------- */
 size_t idlm_isd_accept_workspace_size(int C, int T, int N, int V);
 
