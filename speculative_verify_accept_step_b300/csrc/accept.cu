@@ -16,23 +16,26 @@
 // persistent grid (one CTA per SM) splits the list of 8 KB chunks of all rows
 // evenly; a producer thread streams each CTA's chunks into a 26-stage
 // shared-memory ring with 1-D bulk copies (cp.async.bulk, mbarrier
-// completion), and eight consumer warps each take whole chunks: packed
+// completion), and eleven consumer warps each take whole chunks (copied to registers, so
+// the stage is free again at once): packed
 // bf16x2 maxima per group of 64 values, one exp2 per value for the sum, and
 // the first index of the chunk maximum.  Every chunk leaves one partial
 // (max, sum, max value, argmax) in the workspace; nothing is decided here.
 //
-// Kernels 2 and 3 are launched as programmatic dependents of the kernel
-// before them (they start early and wait in griddepcontrol.wait).
-// Kernel 2 (decide_kernel), one CTA per request, gathers the draft logits
-// before the wait, then combines the request's partials, runs the acceptance
-// scan, writes every output and draws the bonus / fresh token (and
-// SAMPLE-mode proposals): the draw picks the chunk from kernel 1's partial
-// sums and searches only that chunk.  After a rejection at draft j it leaves
-// a decision record instead, and kernel 3 (residual_kernel), one CTA per
-// (request, chunk), sums the residual max(0, p_j - q_j) over each chunk; the
-// last CTA of the request to finish picks the chunk from those sums and
-// searches it.  Kernel-3 CTAs of other requests leave after one read.  Draws
-// are inverse-CDF in vocabulary order.
+// A 13th warp of kernel 1 gathers each request's inputs that do not depend
+// on the pass (draft tokens and their two logits, the proposing rows' (m, S),
+// every Philox uniform) while the logits stream.
+//
+// The decide kernel (one CTA per request), a programmatic dependent of
+// kernel 1, combines the request's chunk partials, runs the acceptance scan,
+// writes every output that needs no draw and appends the open draws to a
+// work list.  The work kernel (a persistent grid, a programmatic dependent
+// of the decide kernel) takes the list: after a rejection at draft j, one
+// item per two chunks sums the residual max(0, p_j - q_j), and the last item
+// of the request to finish picks the chunk from those sums and searches it;
+// otherwise an item draws the bonus / fresh token or a SAMPLE-mode proposal,
+// picking the chunk from kernel 1's partial sums and searching only that
+// chunk.  Draws are inverse-CDF in vocabulary order.
 #include <algorithm>
 #include <mutex>
 
@@ -45,11 +48,13 @@ namespace acc {
 
 constexpr int kItemBytes = 8192;                 // one chunk of a row
 constexpr int kStages = 26;                      // kernel-1 ring depth
-constexpr int kCWarps = 8;                       // kernel-1 consumer warps
-constexpr int kK1Threads = 32 * (kCWarps + 1);
+constexpr int kCWarps = 11;                      // kernel-1 consumer warps
+constexpr int kK1Threads = 32 * (kCWarps + 2);   // + producer warp + request warp
 constexpr size_t kK1Smem = 1024 + size_t(kStages) * kItemBytes + 2 * kStages * 8;
-constexpr int kK2Threads = 128;
-constexpr int kRounds = kItemBytes / 16 / kK2Threads;   // vectors of a chunk per kernel-2 thread
+constexpr int kDThreads = 256;                   // decide kernel
+constexpr int kWThreads = 256;                   // work kernel
+constexpr int kWorkPerSM = 4;                    // work-kernel CTAs per SM
+constexpr int kSliceChunks = 2;                  // chunks per residual slice
 constexpr int kMaxRows = 31;                     // 2N-1 with N <= 16
 constexpr int kMaxChunks = 1024;
 constexpr float kNegInf = -__builtin_inff();
@@ -63,10 +68,28 @@ struct __align__(16) Partial {
   int aidx;    // first index of the max
 };
 
-struct __align__(16) Decision {
-  int residual;         // 1: a rejection whose token comes from the residual
-  int row_p, row_q, n_acc;
-  float mp, isp, mq, isq;
+// Per-request inputs gathered by kernel 1's request warp while the logits
+// stream: draft tokens, their logits in this step's verifying row (xp) and
+// in the previous step's proposing row (yq), the proposing rows' (m, S), and
+// every uniform the request may use.
+struct __align__(16) PreRecord {
+  int dtok[16];
+  float xp[16], yq[16], mq[16], sq[16];
+  float u_acc[16];   // acceptance test of draft i+1
+  float u_draw[16];  // t = 0: bonus / fresh token; t >= 1: SAMPLE proposal t
+  float u_res;       // residual draw
+  int pad[3];
+};
+
+// One unit of the work kernel, written by the decide kernel.
+struct __align__(16) WorkItem {
+  int c, kind, idx, n_acc;   // kind 0: residual slice idx; kind 1: softmax draw t = idx
+  int row_x, row_y;          // residual: rows of p_j (this step) and q_j (previous step);
+                             // draw: the row drawn from (row_y unused)
+  float mx, isx;             // log2-domain max and 1/sum of row x
+  float my, isy;             // the same for row y (residual only)
+  float u;                   // uniform of the draw
+  int pad;
 };
 
 struct Params {
@@ -89,11 +112,13 @@ struct Params {
   float* dbg;
   Partial* part;      // [T][CH]
   float* res_part;    // [C][CH] residual mass per chunk
-  int32_t* res_cnt;   // [C] residual chunks finished (zeroed by kernel 2)
-  Decision* dec;      // [C] acceptance result, kernel 2 -> kernel 3
+  int32_t* res_cnt;   // [C] residual slices finished (zeroed by kernel 1)
+  PreRecord* pre;     // [C] kernel 1 -> decide kernel
+  WorkItem* work;     // [C * max(nslice, N)] decide kernel -> work kernel
+  int32_t* work_cnt;  // [1] items in `work` (zeroed by kernel 1)
   int32_t* status;
   uint64_t seed, step;
-  int V, C, T, N, CH, chunk, greedy, propose, prev_rows;
+  int V, C, T, N, CH, nslice, chunk, greedy, propose, prev_rows;
   float s2;           // log2(e) / T
 };
 
@@ -170,52 +195,112 @@ __device__ __forceinline__ float group_max<float>(const uint4* v) {
 }
 
 // ----------------------------------------------------------------- kernel 1
-//
-// One warp reduces one chunk held in shared memory at `sbase` (cnt values,
-// element e0 of the row first).  Lane l reads vectors l, l+32, ... (no bank
-// conflicts) in groups of 8 vectors; each group updates the lane's running
-// (max, sum) with one rescale and records where the lane's maximum first
-// rose.  The chunk's argmax is found afterwards by re-reading only that
-// group in the lanes that hold the chunk maximum.
+
+// Atomic add at GPU scope with acquire-release ordering: the caller's earlier
+// writes are visible to whoever sees the new count, and the caller sees the
+// writes of everyone who counted before it.
+__device__ __forceinline__ int atomic_add_acq_rel(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Packed fp32x2 arithmetic (two lanes of values per instruction).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Sum of 2^(x s2 - m) over the 8 values of a vector, into two packed
+// accumulators (bf16: one packed FMA, two exp2 and one packed add per pair).
 template <typename T>
-__device__ __forceinline__ Partial consume_chunk(uint32_t sbase, int cnt, int e0, float s2,
-                                                 bool greedy, int lane) {
-  constexpr int EV = Vec<T>::kN;
-  const int nvec = cnt / EV;
-  float m_run = kNegInf, s_run = 0.f, bx = kNegInf;
-  int bg = -1;
-  for (int g0 = 0; g0 < nvec; g0 += 256) {
-    uint4 v[8];
+__device__ __forceinline__ void exp_sum_vec(const uint4& v, uint64_t s2x2, uint64_t nmx2,
+                                            uint64_t& acc0, uint64_t& acc1);
+template <>
+__device__ __forceinline__ void exp_sum_vec<__nv_bfloat16>(const uint4& v, uint64_t s2x2,
+                                                           uint64_t nmx2, uint64_t& acc0,
+                                                           uint64_t& acc1) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int idx = g0 + j * 32 + lane;
-      v[j] = idx < nvec ? lds128(sbase + idx * 16) : Vec<T>::neg_inf();
-    }
-    const float gm = group_max<T>(v);
-    if (gm > bx) {
-      bx = gm;
-      bg = g0;
-    }
-    if (!greedy) {
-      const float mz = gm * s2;
-      if (mz > m_run) {
-        s_run = s_run * fast_exp2(m_run - mz);
-        m_run = mz;
-      }
-      if (m_run > kNegInf) {
-        const float nm = -m_run;
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float x[EV];
-          Vec<T>::get(v[j], x);
-#pragma unroll
-          for (int k = 0; k < EV; ++k) a[k & 3] += fast_exp2(fmaf(x[k], s2, nm));
-        }
-        s_run += (a[0] + a[1]) + (a[2] + a[3]);
-      }
-    }
+  for (int q = 0; q < 4; ++q) {
+    const uint64_t z = fma2(pack2(bf16_lo(w[q]), bf16_hi(w[q])), s2x2, nmx2);
+    float z0, z1;
+    unpack2(z, z0, z1);
+    const uint64_t e = pack2(fast_exp2(z0), fast_exp2(z1));
+    if (q & 1) acc1 = add2(acc1, e);
+    else acc0 = add2(acc0, e);
   }
+}
+template <>
+__device__ __forceinline__ void exp_sum_vec<float>(const uint4& v, uint64_t s2x2, uint64_t nmx2,
+                                                   uint64_t& acc0, uint64_t& acc1) {
+  const uint64_t z0 = fma2(pack2(__uint_as_float(v.x), __uint_as_float(v.y)), s2x2, nmx2);
+  const uint64_t z1 = fma2(pack2(__uint_as_float(v.z), __uint_as_float(v.w)), s2x2, nmx2);
+  float a, b, c, d;
+  unpack2(z0, a, b);
+  unpack2(z1, c, d);
+  acc0 = add2(acc0, pack2(fast_exp2(a), fast_exp2(b)));
+  acc1 = add2(acc1, pack2(fast_exp2(c), fast_exp2(d)));
+}
+
+// Running (max, sum) of one lane over 8 vectors: packed bf16x2 maxima first,
+// one rescale when the lane maximum rises, then one exp2 per value.
+template <typename T>
+__device__ __forceinline__ void lane_group(const uint4* v, float s2, bool greedy, int g,
+                                           float& m_run, uint64_t& acc0, uint64_t& acc1,
+                                           float& bx, int& bg) {
+  const float gm = group_max<T>(v);
+  if (gm > bx) {
+    bx = gm;
+    bg = g;
+  }
+  if (greedy) return;
+  const float mz = gm * s2;
+  if (mz > m_run) {
+    const float f = fast_exp2(m_run - mz);
+    const uint64_t f2 = pack2(f, f), zero = pack2(0.f, 0.f);
+    acc0 = fma2(acc0, f2, zero);
+    acc1 = fma2(acc1, f2, zero);
+    m_run = mz;
+  }
+  if (m_run > kNegInf) {
+    const uint64_t s2x2 = pack2(s2, s2), nmx2 = pack2(-m_run, -m_run);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) exp_sum_vec<T>(v[j], s2x2, nmx2, acc0, acc1);
+  }
+}
+
+// One warp reduces one 8 KB chunk (element e0 of its row first) that it has
+// copied from shared memory into registers: lane l holds vectors
+// l, l+32, ..., l+480 (unused ones hold -inf).  The chunk's argmax is the
+// first index of the chunk maximum among the lanes that hold it.
+template <typename T>
+__device__ __forceinline__ Partial reduce_chunk(const uint4 (&v)[16], int e0, float s2,
+                                                bool greedy, int lane) {
+  constexpr int EV = Vec<T>::kN;
+  float m_run = kNegInf, bx = kNegInf;
+  uint64_t acc0 = pack2(0.f, 0.f), acc1 = acc0;
+  int bg = -1;
+  lane_group<T>(v, s2, greedy, 0, m_run, acc0, acc1, bx, bg);
+  lane_group<T>(v + 8, s2, greedy, 1, m_run, acc0, acc1, bx, bg);
+  float a0, a1, a2, a3;
+  unpack2(acc0, a0, a1);
+  unpack2(acc1, a2, a3);
+  const float s_run = (a0 + a1) + (a2 + a3);
   // (max, sum) over the warp
   float M = m_run;
 #pragma unroll
@@ -230,14 +315,13 @@ __device__ __forceinline__ Partial consume_chunk(uint32_t sbase, int cnt, int e0
   int idx = 0x7fffffff;
   if (bg >= 0 && bx == BX) {
 #pragma unroll
-    for (int j = 7; j >= 0; --j) {
-      const int vi = bg + j * 32 + lane;
-      if (vi < nvec) {
+    for (int j = 15; j >= 0; --j) {
+      if ((j >> 3) == bg) {
         float x[EV];
-        Vec<T>::get(lds128(sbase + vi * 16), x);
+        Vec<T>::get(v[j], x);
 #pragma unroll
         for (int k = EV - 1; k >= 0; --k)
-          if (x[k] == BX) idx = vi * EV + k;
+          if (x[k] == BX) idx = (j * 32 + lane) * EV + k;
       }
     }
   }
@@ -249,6 +333,65 @@ __device__ __forceinline__ Partial consume_chunk(uint32_t sbase, int cnt, int e0
   pt.amax = BX;
   pt.aidx = idx == 0x7fffffff ? idx : e0 + idx;
   return pt;
+}
+
+// Layout of request c as its inputs state it; false if they disagree.
+struct Layout {
+  int row0, rows, ncl, prow0;
+  bool full;
+};
+__device__ __forceinline__ bool request_layout(const Params& p, int c, Layout& L) {
+  const int M = p.N - 1;
+  L.row0 = p.qo[c];
+  L.rows = p.qo[c + 1] - L.row0;
+  L.full = p.mode[c] == IDLM_MODE_FULL;
+  L.ncl = L.full ? p.N : 1;
+  L.prow0 = L.full ? p.prev_row0[c] : 0;
+  return L.rows == L.ncl + M && L.row0 >= 0 && L.row0 + L.rows <= p.T &&
+         (!L.full || (L.prow0 >= 0 && L.prow0 + M <= p.prev_rows));
+}
+
+// Kernel 1's request warp: everything request c needs that does not depend
+// on the vocab pass (one warp; lanes in parallel).
+template <typename T>
+__device__ void request_inputs(const Params& p, int c, int lane) {
+  const int N = p.N, M = N - 1, V = p.V;
+  PreRecord* pr = p.pre + c;
+  Layout L;
+  const bool ok = request_layout(p, c, L);
+  if (lane == 0) p.res_cnt[c] = 0;
+  if (lane == 0 && c == 0) *p.work_cnt = 0;
+  if (!ok) {
+    if (lane == 0) set_status(p.status, IDLM_DEV_BAD_LAYOUT);
+    return;
+  }
+  if (lane < M) {
+    int d = -1;
+    float xp = 0.f, yq = 0.f, mq = 0.f, sq = 1.f;
+    if (L.full) {
+      d = p.drafts[c * M + lane];
+      mq = p.dq_stats[2 * (c * M + lane)];
+      sq = p.dq_stats[2 * (c * M + lane) + 1];
+      if (d >= 0 && d < V) {
+        xp = load1(static_cast<const T*>(p.logits) + static_cast<size_t>(L.row0 + lane) * V + d);
+        yq = load1(static_cast<const T*>(p.prev_logits) + static_cast<size_t>(L.prow0 + lane) * V + d);
+      } else {
+        set_status(p.status, IDLM_DEV_BAD_TOKEN);
+      }
+    }
+    pr->dtok[lane] = d;
+    pr->xp[lane] = xp;
+    pr->yq[lane] = yq;
+    pr->mq[lane] = mq;
+    pr->sq[lane] = sq;
+    pr->u_acc[lane] = isd_uniform(p.seed, p.step, c, kPurposeAccept, lane);
+  }
+  if (lane >= 16 && lane < 16 + N) {
+    const int t = lane - 16;
+    pr->u_draw[t] = t == 0 ? isd_uniform(p.seed, p.step, c, kPurposeSample, 0)
+                           : isd_uniform(p.seed, p.step, c, kPurposePropose, t - 1);
+  }
+  if (lane == 31) pr->u_res = isd_uniform(p.seed, p.step, c, kPurposeSample, 1);
 }
 
 template <typename T>
@@ -276,6 +419,11 @@ __global__ void __launch_bounds__(kK1Threads, 1) vocab_stream_kernel(const Param
   const int n = static_cast<int>(hi - lo);
   const T* logits = static_cast<const T*>(p.logits);
 
+  if (warp == kCWarps + 1) {
+    // ------------------------------------------------------ request warp
+    for (int c = blockIdx.x; c < p.C; c += gridDim.x) request_inputs<T>(p, c, lane);
+    return;
+  }
   if (warp == kCWarps) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
@@ -315,14 +463,19 @@ __global__ void __launch_bounds__(kK1Threads, 1) vocab_stream_kernel(const Param
     if (!mbar_wait_bounded(&full[s], ph, &abort_flag, p.status)) break;
     const size_t item = static_cast<size_t>(row) * p.CH + ch;
     const int e0 = ch * p.chunk;
-    const int cnt = min(p.chunk, p.V - e0);
-    const Partial pt =
-        consume_chunk<T>(smem_u32(base + size_t(s) * kItemBytes), cnt, e0, p.s2, p.greedy, lane);
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&empty[s]);
-      p.part[item] = pt;
+    const int nvec = min(p.chunk, p.V - e0) / Vec<T>::kN;
+    // copy the chunk to registers and hand the stage back at once
+    const uint32_t sb = smem_u32(base + size_t(s) * kItemBytes);
+    uint4 v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int idx = q * 32 + lane;
+      v[q] = idx < nvec ? lds128(sb + idx * 16) : Vec<T>::neg_inf();
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    const Partial pt = reduce_chunk<T>(v, e0, p.s2, p.greedy, lane);
+    if (lane == 0) p.part[item] = pt;
   }
 }
 
@@ -340,21 +493,22 @@ struct WeightFn {
   }
 };
 
+constexpr int kMaxRounds = 4;       // vectors of a chunk per thread in a search
+constexpr int kMaxWarps = 8;
+
 struct DecideSmem {
   float rm[kMaxRows], rs[kMaxRows];
   int ridx[kMaxRows];
-  float xp[16], yq[16];
-  int dtok[16];
   int acc_ok[16];
-  float mass[kMaxChunks];
-  float red[kRounds][kK2Threads / 32];
+  float red[kMaxRounds][kMaxWarps];
   int found, last_pos;
   int pick_ch;
   float pick_off;
-  int n_acc;
-  int is_last;
+  int flag;
+  float mass[kMaxChunks];
 };
 
+template <int THREADS>
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -363,54 +517,49 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   if (l == 0) red[w] = v;
   __syncthreads();
   v = 0.f;
-  for (int i = 0; i < kK2Threads / 32; ++i) v += red[i];
+#pragma unroll
+  for (int i = 0; i < THREADS / 32; ++i) v += red[i];
   return v;
-}
-
-// Weights of the values in vector `vi` of a chunk (row y optional).
-template <typename T>
-__device__ __forceinline__ void vec_weights(const uint4* xs, const uint4* ys, int vi,
-                                            const WeightFn& wf, float* w) {
-  constexpr int EV = Vec<T>::kN;
-  float x[EV], y[EV];
-  Vec<T>::get(__ldg(xs + vi), x);
-  if (ys) {
-    Vec<T>::get(__ldg(ys + vi), y);
-  } else {
-#pragma unroll
-    for (int k = 0; k < EV; ++k) y[k] = 0.f;
-  }
-#pragma unroll
-  for (int k = 0; k < EV; ++k) w[k] = wf(x[k], y[k]);
 }
 
 // Inverse CDF inside one chunk (global memory, `cnt` values from xs[0]):
 // the first element in index order whose running weight sum exceeds
 // `target`; if rounding leaves none, the last element with positive weight.
-// Element order is (round k, thread t, value): round k covers vectors
-// [128k, 128k + 128).  Adjacent intervals share their boundary value bit for
-// bit, so no target falls in a gap.  Every thread returns the answer
-// (chunk-relative index, or -1 if every weight is zero).
-template <typename T>
+// Element order is (round r, thread t, value): round r covers vectors
+// [THREADS r, THREADS (r + 1)).  Adjacent intervals share their boundary
+// value bit for bit, so no target falls in a gap.  Every thread returns the
+// answer (chunk-relative index, or -1 if every weight is zero).
+template <typename T, int THREADS>
 __device__ int chunk_search(const uint4* xs, const uint4* ys, int cnt, float target,
                             const WeightFn& wf, DecideSmem& sm) {
   constexpr int EV = Vec<T>::kN;
+  constexpr int R = kItemBytes / 16 / THREADS;
+  constexpr int NW = THREADS / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nvec = cnt / EV;
-  float w[kRounds][EV];
-  float inc[kRounds], exc[kRounds];
+  float w[R][EV];
+  float inc[R], exc[R];
+  {
+    // every load of the chunk in flight before any weight is computed
+    uint4 vx[R], vy[R];
 #pragma unroll
-  for (int k = 0; k < kRounds; ++k) {
-    const int vi = k * kK2Threads + tid;
-    if (vi < nvec) {
-      vec_weights<T>(xs, ys, vi, wf, w[k]);
-    } else {
+    for (int k = 0; k < R; ++k) {
+      const int vi = k * THREADS + tid;
+      vx[k] = vi < nvec ? __ldg(xs + vi) : make_uint4(0u, 0u, 0u, 0u);
+      vy[k] = (ys && vi < nvec) ? __ldg(ys + vi) : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-      for (int e = 0; e < EV; ++e) w[k][e] = 0.f;
+    for (int k = 0; k < R; ++k) {
+      const int vi = k * THREADS + tid;
+      float x[EV], y[EV];
+      Vec<T>::get(vx[k], x);
+      Vec<T>::get(vy[k], y);
+#pragma unroll
+      for (int e = 0; e < EV; ++e) w[k][e] = vi < nvec ? wf(x[e], y[e]) : 0.f;
     }
   }
 #pragma unroll
-  for (int k = 0; k < kRounds; ++k) {
+  for (int k = 0; k < R; ++k) {
     float t = 0.f;
 #pragma unroll
     for (int e = 0; e < EV; ++e) t += w[k][e];
@@ -430,19 +579,21 @@ __device__ int chunk_search(const uint4* xs, const uint4* ys, int cnt, float tar
   __syncthreads();
   if (lane == 31)
 #pragma unroll
-    for (int k = 0; k < kRounds; ++k) sm.red[k][warp] = inc[k];
+    for (int k = 0; k < R; ++k) sm.red[k][warp] = inc[k];
   __syncthreads();
   float base = 0.f;
+  int last = -1;
 #pragma unroll
-  for (int k = 0; k < kRounds; ++k) {
+  for (int k = 0; k < R; ++k) {
     float before = 0.f, total = 0.f;
-    for (int i = 0; i < kK2Threads / 32; ++i) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
       if (i == warp) before = total;
       total += sm.red[k][i];
     }
     const float lo = base + (before + exc[k]);
     const float hi = base + (before + inc[k]);
-    const int vi = k * kK2Threads + tid;
+    const int vi = k * THREADS + tid;
     if (lo <= target && target < hi) {
       float acc = lo;
       int pick = -1;
@@ -459,82 +610,138 @@ __device__ int chunk_search(const uint4* xs, const uint4* ys, int cnt, float tar
 #pragma unroll
     for (int e = EV - 1; e >= 0; --e)
       if (w[k][e] > 0.f) {
-        atomicMax(&sm.last_pos, vi * EV + e);
+        last = max(last, vi * EV + e);
         break;
       }
     base = base + total;
   }
+  // last element with positive weight: one shared atomic per warp
+#pragma unroll
+  for (int o = 16; o; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  if (lane == 0 && last >= 0) atomicMax(&sm.last_pos, last);
   __syncthreads();
   const int r = sm.found != 0x7fffffff ? sm.found : sm.last_pos;
   __syncthreads();
   return r;
 }
 
-// Walk the chunk masses in order: chunk holding u * total and the offset
-// into it.  Thread 0 only.
-__device__ __forceinline__ void pick_chunk(const float* mass, int CH, float u, int* ch_out,
-                                           float* off_out) {
-  float total = 0.f;
-  for (int k = 0; k < CH; ++k) total += mass[k];
-  const float target = u * total;
-  float acc = 0.f;
+// Chunk holding u * total of the masses, and the offset into it: the first
+// chunk k with positive mass whose running sum (index order) exceeds the
+// target; if rounding leaves none, the last chunk with positive mass.  One
+// warp: lane l holds a contiguous run of chunks, so lane order is index
+// order.  Writes sm.pick_ch / sm.pick_off (read them after a barrier).
+__device__ __forceinline__ float pick_chunk_warp(const float* mass, int CH, float u,
+                                                 DecideSmem& sm) {
+  const int lane = threadIdx.x & 31;
+  const int per = (CH + 31) / 32;
+  const int k0 = min(CH, lane * per), k1 = min(CH, k0 + per);
+  float mine = 0.f;
   int last = -1;
-  for (int k = 0; k < CH; ++k) {
-    if (mass[k] > 0.f) {
-      if (acc + mass[k] > target) {
-        *ch_out = k;
-        *off_out = target - acc;
-        return;
+  for (int k = k0; k < k1; ++k) {
+    mine += mass[k];
+    if (mass[k] > 0.f) last = k;
+  }
+  float inc = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float nb = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += nb;
+  }
+  const float total = __shfl_sync(0xffffffffu, inc, 31);
+  const float target = u * total;
+  float acc = inc - mine;   // sum before this lane's run
+  int pick = -1;
+  float off = 0.f;
+  if (acc <= target && target < inc) {
+    for (int k = k0; k < k1; ++k) {
+      if (mass[k] > 0.f && acc + mass[k] > target) {
+        pick = k;
+        off = target - acc;
+        break;
       }
-      last = k;
+      acc += mass[k];
     }
-    acc += mass[k];
+    if (pick < 0 && last >= 0) {   // rounding inside the run: its last positive chunk
+      pick = last;
+      off = mass[last];
+    }
   }
-  *ch_out = last < 0 ? 0 : last;
-  *off_out = last < 0 ? 0.f : mass[last];
+  // first lane with a pick; else the last positive chunk
+  const unsigned hit = __ballot_sync(0xffffffffu, pick >= 0);
+  if (hit) {
+    const int src = __ffs(hit) - 1;
+    pick = __shfl_sync(0xffffffffu, pick, src);
+    off = __shfl_sync(0xffffffffu, off, src);
+  } else {
+    int lp = last;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+    pick = lp < 0 ? 0 : lp;
+    off = lp < 0 ? 0.f : mass[lp];
+  }
+  if (lane == 0) {
+    sm.pick_ch = pick;
+    sm.pick_off = off;
+  }
+  return total;
 }
 
-// Softmax masses of the chunks of one row from kernel 1's partials.
-__device__ __forceinline__ void row_masses(const Params& p, int row, float m, DecideSmem& sm) {
-  const float4* pr = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(row) * p.CH);
-  for (int k = threadIdx.x; k < p.CH; k += kK2Threads) {
-    const float4 q = __ldcg(pr + k);
-    sm.mass[k] = q.y * fast_exp2(q.x - m);
-  }
-  __syncthreads();
-}
-
-// Inverse-CDF draw from the softmax of `row` (row max m, log2 domain): pick
-// the chunk from the partial masses, then search that chunk.
-template <typename T>
-__device__ int draw_softmax(const Params& p, const T* rowp, int row, float m, float u,
+// Inverse-CDF draw from the softmax of `row` (row max m, log2 domain), with
+// the chunk masses already in `mass`: pick the chunk, then search it.
+template <typename T, int THREADS>
+__device__ int draw_softmax(const Params& p, const T* rowp, const float* mass, float m, float u,
                             DecideSmem& sm) {
-  row_masses(p, row, m, sm);
-  if (threadIdx.x == 0) pick_chunk(sm.mass, p.CH, u, &sm.pick_ch, &sm.pick_off);
+  if (threadIdx.x < 32) pick_chunk_warp(mass, p.CH, u, sm);
   __syncthreads();
   const int ch = sm.pick_ch;
   const float target = sm.pick_off;
   const int e0 = ch * p.chunk;
   const WeightFn wp{0, p.s2, m, 0.f, 1.f, 0.f, 1.f};
-  const int e = chunk_search<T>(reinterpret_cast<const uint4*>(rowp + e0), nullptr,
-                                min(p.chunk, p.V - e0), target, wp, sm);
+  const int e = chunk_search<T, THREADS>(reinterpret_cast<const uint4*>(rowp + e0), nullptr,
+                                         min(p.chunk, p.V - e0), target, wp, sm);
   return e >= 0 ? e0 + e : 0;
 }
 
-// (max, sum, argmax) of one row from its chunk partials: one warp.
+// Softmax masses of the chunks of one row from kernel 1's partials.
+template <int THREADS>
+__device__ __forceinline__ void row_masses(const Params& p, int row, float m, float* mass) {
+  const float4* pr = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(row) * p.CH);
+  for (int k = threadIdx.x; k < p.CH; k += THREADS) {
+    const float4 q = __ldcg(pr + k);
+    mass[k] = q.y * fast_exp2(q.x - m);
+  }
+  __syncthreads();
+}
+
+// (max, sum, argmax) of one row from its chunk partials: one warp, one round
+// of loads for up to 128 chunks.
 __device__ __forceinline__ void combine_row(const Params& p, int row, int i, DecideSmem& sm) {
   const int lane = threadIdx.x & 31;
   const float4* pr = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(row) * p.CH);
-  float m = kNegInf;
-  for (int k = lane; k < p.CH; k += 32) m = fmaxf(m, __ldcg(pr + k).x);
+  float4 q[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int k = lane + 32 * r;
+    q[r] = k < p.CH ? __ldcg(pr + k) : make_float4(kNegInf, 0.f, kNegInf, __int_as_float(0x7fffffff));
+  }
+  float m = fmaxf(fmaxf(q[0].x, q[1].x), fmaxf(q[2].x, q[3].x));
+  for (int k = lane + 128; k < p.CH; k += 32) m = fmaxf(m, __ldcg(pr + k).x);
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float s = 0.f, av = kNegInf;
   int ai = 0x7fffffff;
-  for (int k = lane; k < p.CH; k += 32) {
-    const float4 q = __ldcg(pr + k);   // (m, s, amax, aidx); an L1 hit after the first loop
-    s += q.y * fast_exp2(q.x - m);
-    argmax_merge(av, ai, q.z, __float_as_int(q.w));
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int k = lane + 32 * r;
+    if (k < p.CH) {
+      s += q[r].y * fast_exp2(q[r].x - m);
+      argmax_merge(av, ai, q[r].z, __float_as_int(q[r].w));
+    }
+  }
+  for (int k = lane + 128; k < p.CH; k += 32) {
+    const float4 t = __ldcg(pr + k);
+    s += t.y * fast_exp2(t.x - m);
+    argmax_merge(av, ai, t.z, __float_as_int(t.w));
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -550,69 +757,53 @@ __device__ __forceinline__ void combine_row(const Params& p, int row, int i, Dec
   }
 }
 
-// Kernel 2: one CTA per request.  Combines the request's chunk partials,
-// runs the acceptance scan, writes every output except a residual token and
-// the decision record for kernel 3, then draws the bonus / fresh token and
-// any SAMPLE-mode proposals (nothing is drawn after a rejection here).
+// Decide kernel: one CTA per request, launched as a programmatic dependent
+// of kernel 1.  Combines the request's chunk partials (one warp per row, one
+// round of loads), runs the acceptance scan, writes every output that needs
+// no draw, and appends the draws it leaves open to the work list: after a
+// rejection at draft j, one residual slice per two chunks of p_j / q_j;
+// otherwise the bonus / fresh token and any SAMPLE-mode proposals.
 template <typename T>
-__global__ void __launch_bounds__(kK2Threads) decide_kernel(const Params p) {
+__global__ void __launch_bounds__(kDThreads) decide_kernel(const Params p) {
   __shared__ DecideSmem sm;
+  __shared__ int base;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int c = blockIdx.x;
   const int N = p.N, M = N - 1, V = p.V;
-  const T* logits = static_cast<const T*>(p.logits);
-  const T* prev = static_cast<const T*>(p.prev_logits);
   griddep_launch_dependents();
-
-  const int row0 = p.qo[c];
-  const int rows = p.qo[c + 1] - row0;
-  const bool full = p.mode[c] == IDLM_MODE_FULL;
-  const int ncl = full ? N : 1;
-  const int prow0 = full ? p.prev_row0[c] : 0;
-  if (rows != ncl + M || row0 < 0 || row0 + rows > p.T ||
-      (full && (prow0 < 0 || prow0 + M > p.prev_rows))) {
-    if (tid == 0) {
-      set_status(p.status, IDLM_DEV_BAD_LAYOUT);
-      p.dec[c].residual = 0;
-    }
-    return;
-  }
-  // draft logits and q statistics: inputs of this call, not kernel 1's
-  // results, so they are read before waiting for kernel 1
-  float mq_i = 0.f, sq_i = 1.f;
-  if (full && tid < M) {
-    const int d = p.drafts[c * M + tid];
-    sm.dtok[tid] = d;
-    mq_i = p.dq_stats[2 * (c * M + tid)];
-    sq_i = p.dq_stats[2 * (c * M + tid) + 1];
-    if (d >= 0 && d < V) {
-      sm.xp[tid] = load1(logits + static_cast<size_t>(row0 + tid) * V + d);
-      sm.yq[tid] = load1(prev + static_cast<size_t>(prow0 + tid) * V + d);
-    }
-  }
+  Layout L;
+  if (!request_layout(p, c, L)) return;   // kernel 1 has set the status
+  const int ncl = L.ncl;
   if (tid < 16) sm.acc_ok[tid] = 0;
   griddep_wait();
 
-  // 1. row statistics of every row of the request
-  for (int i = warp; i < rows; i += kK2Threads / 32) combine_row(p, row0 + i, i, sm);
+  // kernel 1's request record and the row partials, in one round
+  const PreRecord* pr = p.pre + c;
+  int d = -1;
+  float u = 0.f, mq = 0.f, sq = 1.f, xp = 0.f, yq = 0.f;
+  if (L.full && tid < M) {
+    d = pr->dtok[tid];
+    u = pr->u_acc[tid];
+    mq = pr->mq[tid];
+    sq = pr->sq[tid];
+    xp = pr->xp[tid];
+    yq = pr->yq[tid];
+  }
+  for (int i = warp; i < L.rows; i += kDThreads / 32) combine_row(p, L.row0 + i, i, sm);
   __syncthreads();
 
-  // 2. verification of the drafts (FULL)
-  if (full && tid < M) {
+  // verification of the drafts (FULL)
+  if (L.full && tid < M) {
     const int i = tid;   // draft i+1, verified by clean row i
-    const int d = sm.dtok[i];
-    const float u = isd_uniform(p.seed, p.step, c, kPurposeAccept, i);
     float pv = 0.f, qv = 0.f, ratio = 0.f;
     int ok = 0;
-    if (d < 0 || d >= V) {
-      set_status(p.status, IDLM_DEV_BAD_TOKEN);
-    } else {
+    if (d >= 0 && d < V) {
       if (p.greedy) {
         pv = (d == sm.ridx[i]) ? 1.f : 0.f;
-        qv = (sm.yq[i] == mq_i) ? 1.f : 0.f;
+        qv = (yq == mq) ? 1.f : 0.f;
       } else {
-        pv = fast_exp2(sm.xp[i] * p.s2 - sm.rm[i]) / sm.rs[i];
-        qv = fast_exp2(sm.yq[i] * p.s2 - mq_i * kLog2e) / sq_i;
+        pv = fast_exp2(xp * p.s2 - sm.rm[i]) / sm.rs[i];
+        qv = fast_exp2(yq * p.s2 - mq * kLog2e) / sq;
       }
       ratio = qv > 0.f ? pv / qv : kInf;
       ok = u < fminf(1.f, ratio);
@@ -627,50 +818,65 @@ __global__ void __launch_bounds__(kK2Threads) decide_kernel(const Params p) {
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    int n = 0;
-    if (full)
-      while (n < M && sm.acc_ok[n]) ++n;
-    sm.n_acc = n;
-  }
-  __syncthreads();
-  const int n_acc = sm.n_acc;
-  const bool rejected = full && n_acc < M;
+  int n_acc = 0;
+  if (L.full)
+    while (n_acc < M && sm.acc_ok[n_acc]) ++n_acc;
+  const bool rejected = L.full && n_acc < M;
+  const bool residual = rejected && !p.greedy;
+  const int ndraw = (rejected || p.greedy) ? 0 : (p.propose == IDLM_PROPOSE_SAMPLE ? N : 1);
+  const int nitems = residual ? p.nslice : ndraw;
 
-  // 3. the decision record and every output that needs no draw
-  if (tid == 0) {
-    Decision dr;
-    dr.residual = rejected && !p.greedy;
-    dr.row_p = row0 + n_acc;
-    dr.row_q = prow0 + n_acc;
-    dr.n_acc = n_acc;
-    dr.mp = sm.rm[n_acc];
-    dr.isp = 1.f / sm.rs[n_acc];
-    dr.mq = 0.f;
-    dr.isq = 1.f;
-    if (dr.residual) {
-      dr.mq = p.dq_stats[2 * (c * M + n_acc)] * kLog2e;
-      dr.isq = 1.f / p.dq_stats[2 * (c * M + n_acc) + 1];
+  // work items for the draws left open
+  if (tid == 0 && nitems) base = atomicAdd(p.work_cnt, nitems);
+  __syncthreads();
+  if (tid < nitems) {
+    WorkItem it;
+    it.c = c;
+    it.idx = tid;
+    it.n_acc = n_acc;
+    it.pad = 0;
+    if (residual) {
+      it.kind = 0;
+      it.row_x = L.row0 + n_acc;
+      it.row_y = L.prow0 + n_acc;
+      it.mx = sm.rm[n_acc];
+      it.isx = 1.f / sm.rs[n_acc];
+      it.my = pr->mq[n_acc] * kLog2e;
+      it.isy = 1.f / pr->sq[n_acc];
+      it.u = pr->u_res;
+    } else {
+      const int li = tid == 0 ? ncl - 1 : ncl + tid - 1;
+      it.kind = 1;
+      it.row_x = L.row0 + li;
+      it.row_y = 0;
+      it.mx = sm.rm[li];
+      it.isx = 1.f / sm.rs[li];
+      it.my = 0.f;
+      it.isy = 1.f;
+      it.u = pr->u_draw[tid];
     }
-    p.dec[c] = dr;
-    p.res_cnt[c] = 0;
+    p.work[base + tid] = it;
+  }
+
+  // every output that needs no draw
+  if (tid == 0) {
     p.n_accepted[c] = n_acc;
     p.n_out[c] = n_acc + 1;
-    p.n_commit[c] = full ? 1 + n_acc : 1;
+    p.n_commit[c] = L.full ? 1 + n_acc : 1;
     p.next_mode[c] = rejected ? IDLM_MODE_FRESH : IDLM_MODE_FULL;
-    p.next_mask_row0[c] = row0 + ncl;
+    p.next_mask_row0[c] = L.row0 + ncl;
   }
   const float to_nat = p.greedy ? 1.f : (1.f / kLog2e);
-  if (p.row_stats && tid < rows) {
-    p.row_stats[2 * (row0 + tid)] = sm.rm[tid] * to_nat;
-    p.row_stats[2 * (row0 + tid) + 1] = sm.rs[tid];
+  if (p.row_stats && tid < L.rows) {
+    p.row_stats[2 * (L.row0 + tid)] = sm.rm[tid] * to_nat;
+    p.row_stats[2 * (L.row0 + tid) + 1] = sm.rs[tid];
   }
   if (tid < M) {
     p.next_q_stats[2 * (c * M + tid)] = sm.rm[ncl + tid] * to_nat;
     p.next_q_stats[2 * (c * M + tid) + 1] = sm.rs[ncl + tid];
   }
   if (tid < N) {
-    if (tid < n_acc) p.out_tokens[c * N + tid] = sm.dtok[tid];
+    if (tid < n_acc) p.out_tokens[c * N + tid] = pr->dtok[tid];
     else if (tid > n_acc) p.out_tokens[c * N + tid] = -1;
     else if (p.greedy) p.out_tokens[c * N + tid] = sm.ridx[rejected ? n_acc : ncl - 1];
   }
@@ -679,93 +885,121 @@ __global__ void __launch_bounds__(kK2Threads) decide_kernel(const Params p) {
     else if (p.greedy || p.propose == IDLM_PROPOSE_ARGMAX)
       p.next_drafts[c * M + tid] = sm.ridx[ncl + tid];
   }
-
-  // 4. draws from p: bonus / fresh token (t = 0), SAMPLE proposals (t >= 1)
-  if (!rejected && !p.greedy) {
-    const int ntask = p.propose == IDLM_PROPOSE_SAMPLE ? N : 1;
-    for (int t = 0; t < ntask; ++t) {
-      const int li = t == 0 ? ncl - 1 : ncl + t - 1;
-      const float u = t == 0 ? isd_uniform(p.seed, p.step, c, kPurposeSample, 0)
-                             : isd_uniform(p.seed, p.step, c, kPurposePropose, t - 1);
-      const int tok = draw_softmax<T>(p, logits + static_cast<size_t>(row0 + li) * V, row0 + li,
-                                      sm.rm[li], u, sm);
-      if (tid == 0) {
-        if (t == 0) p.out_tokens[c * N + n_acc] = tok;
-        else p.next_drafts[c * M + t - 1] = tok;
-      }
-    }
-  }
 }
 
-// Kernel 3: one CTA per (request, chunk).  For a request rejected at draft
-// j, CTA k sums the residual max(0, p_j - q_j) over chunk k; the last CTA of
-// the request to finish picks the chunk from those sums and searches it (or
-// draws from p_j when the residual is zero everywhere).  Every other CTA
-// leaves after reading the decision record.
+// Work kernel: a persistent grid (kWorkPerSM CTAs per SM), launched as a
+// programmatic dependent of the decide kernel, takes the work list in order.
+// A residual slice sums max(0, p_j - q_j) over its two chunks; the last
+// slice of a request to finish picks the chunk from the sums and searches it
+// (or draws from p_j when the residual is zero everywhere).  A softmax draw
+// picks the chunk from kernel 1's partial sums and searches only that chunk.
 template <typename T>
-__global__ void __launch_bounds__(kK2Threads) residual_kernel(const Params p) {
+__global__ void __launch_bounds__(kWThreads) work_kernel(const Params p) {
   __shared__ DecideSmem sm;
-  __shared__ Decision dr;
-  const int tid = threadIdx.x;
-  const int c = blockIdx.x / p.CH;
-  const int k = blockIdx.x % p.CH;
-  const int V = p.V;
-  griddep_wait();
-  if (tid == 0) dr = p.dec[c];
-  __syncthreads();
-  if (!dr.residual) return;
-  const T* rp = static_cast<const T*>(p.logits) + static_cast<size_t>(dr.row_p) * V;
-  const T* rq = static_cast<const T*>(p.prev_logits) + static_cast<size_t>(dr.row_q) * V;
-  const WeightFn wres{1, p.s2, 0.f, dr.mp, dr.isp, dr.mq, dr.isq};
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int N = p.N, M = N - 1, V = p.V;
+  const T* logits = static_cast<const T*>(p.logits);
   constexpr int EV = Vec<T>::kN;
-  const int e0 = k * p.chunk;
-  const int nvec = min(p.chunk, V - e0) / EV;
-  const uint4* xs = reinterpret_cast<const uint4*>(rp + e0);
-  const uint4* ys = reinterpret_cast<const uint4*>(rq + e0);
-  float acc = 0.f;
-#pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    const int vi = r * kK2Threads + tid;
-    if (vi < nvec) {
-      float w[EV];
-      vec_weights<T>(xs, ys, vi, wres, w);
-#pragma unroll
-      for (int e = 0; e < EV; ++e) acc += w[e];
+  constexpr int R = kItemBytes / 16 / kWThreads;
+  griddep_wait();
+  const int count = __ldcg(p.work_cnt);
+  for (int i = blockIdx.x; i < count; i += gridDim.x) {
+    const WorkItem it = p.work[i];
+    const int c = it.c;
+    const T* rx = logits + static_cast<size_t>(it.row_x) * V;
+    if (it.kind == 1) {
+      row_masses<kWThreads>(p, it.row_x, it.mx, sm.mass);
+      const int tok = draw_softmax<T, kWThreads>(p, rx, sm.mass, it.mx, it.u, sm);
+      if (tid == 0) {
+        if (it.idx == 0) p.out_tokens[c * N + it.n_acc] = tok;
+        else p.next_drafts[c * M + it.idx - 1] = tok;
+      }
+      __syncthreads();
+      continue;
     }
+    // residual slice idx over chunks [2 idx, 2 idx + 2)
+    const T* ry = static_cast<const T*>(p.prev_logits) + static_cast<size_t>(it.row_y) * V;
+    const WeightFn wres{1, p.s2, 0.f, it.mx, it.isx, it.my, it.isy};
+    const int ch0 = it.idx * kSliceChunks;
+    float part[kSliceChunks];
+    {
+      uint4 vx[kSliceChunks][R], vy[kSliceChunks][R];
+#pragma unroll
+      for (int h = 0; h < kSliceChunks; ++h) {
+        const int ch = ch0 + h;
+        const int e0 = ch * p.chunk;
+        const int nvec = ch < p.CH ? min(p.chunk, V - e0) / EV : 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int vi = r * kWThreads + tid;
+          vx[h][r] = vi < nvec ? __ldg(reinterpret_cast<const uint4*>(rx + e0) + vi) : make_uint4(0u, 0u, 0u, 0u);
+          vy[h][r] = vi < nvec ? __ldg(reinterpret_cast<const uint4*>(ry + e0) + vi) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kSliceChunks; ++h) {
+        const int ch = ch0 + h;
+        const int nvec = ch < p.CH ? min(p.chunk, V - ch * p.chunk) / EV : 0;
+        float a = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (r * kWThreads + tid < nvec) {
+            float x[EV], y[EV];
+            Vec<T>::get(vx[h][r], x);
+            Vec<T>::get(vy[h][r], y);
+#pragma unroll
+            for (int e = 0; e < EV; ++e) a += wres(x[e], y[e]);
+          }
+        }
+        part[h] = a;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kSliceChunks; ++h) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) part[h] += __shfl_xor_sync(0xffffffffu, part[h], o);
+    }
+    if ((tid & 31) == 0)
+#pragma unroll
+      for (int h = 0; h < kSliceChunks; ++h) sm.red[h][warp] = part[h];
+    __syncthreads();
+    if (tid < kSliceChunks && ch0 + tid < p.CH) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWThreads / 32; ++w) a += sm.red[tid][w];
+      p.res_part[static_cast<size_t>(c) * p.CH + ch0 + tid] = a;
+      __threadfence();
+    }
+    __syncthreads();
+    if (tid == 0) sm.flag = atomic_add_acq_rel(&p.res_cnt[c], 1) == p.nslice - 1;
+    __syncthreads();
+    if (!sm.flag) continue;
+    // the last slice of the request: every chunk's mass is visible now
+    for (int j = tid; j < p.CH; j += kWThreads)
+      sm.mass[j] = __ldcg(p.res_part + static_cast<size_t>(c) * p.CH + j);
+    __syncthreads();
+    if (tid < 32) {
+      const float tot = pick_chunk_warp(sm.mass, p.CH, it.u, sm);
+      if (tid == 0) sm.flag = tot > 0.f;
+    }
+    __syncthreads();
+    int tok;
+    if (sm.flag) {
+      const int ch = sm.pick_ch;
+      const float target = sm.pick_off;
+      const int f0 = ch * p.chunk;
+      const int e = chunk_search<T, kWThreads>(reinterpret_cast<const uint4*>(rx + f0),
+                                               reinterpret_cast<const uint4*>(ry + f0),
+                                               min(p.chunk, V - f0), target, wres, sm);
+      tok = e >= 0 ? f0 + e : 0;
+    } else {
+      // p_j == q_j everywhere: draw from p_j
+      row_masses<kWThreads>(p, it.row_x, it.mx, sm.mass);
+      tok = draw_softmax<T, kWThreads>(p, rx, sm.mass, it.mx, it.u, sm);
+    }
+    if (tid == 0) p.out_tokens[c * N + it.n_acc] = tok;
+    __syncthreads();
   }
-  acc = block_sum(acc, sm.red[0]);
-  if (tid == 0) {
-    p.res_part[static_cast<size_t>(c) * p.CH + k] = acc;
-    __threadfence();
-    sm.is_last = atomicAdd(&p.res_cnt[c], 1) == p.CH - 1;
-  }
-  __syncthreads();
-  if (!sm.is_last) return;
-  __threadfence();
-  const float u = isd_uniform(p.seed, p.step, c, kPurposeSample, 1);
-  for (int j = tid; j < p.CH; j += kK2Threads)
-    sm.mass[j] = __ldcg(p.res_part + static_cast<size_t>(c) * p.CH + j);
-  __syncthreads();
-  if (tid == 0) {
-    float tot = 0.f;
-    for (int j = 0; j < p.CH; ++j) tot += sm.mass[j];
-    sm.n_acc = tot > 0.f;
-    if (tot > 0.f) pick_chunk(sm.mass, p.CH, u, &sm.pick_ch, &sm.pick_off);
-  }
-  __syncthreads();
-  int tok;
-  if (sm.n_acc) {
-    const int ch = sm.pick_ch;
-    const float target = sm.pick_off;
-    const int f0 = ch * p.chunk;
-    const int e = chunk_search<T>(reinterpret_cast<const uint4*>(rp + f0),
-                                  reinterpret_cast<const uint4*>(rq + f0), min(p.chunk, V - f0),
-                                  target, wres, sm);
-    tok = e >= 0 ? f0 + e : 0;
-  } else {
-    tok = draw_softmax<T>(p, rp, dr.row_p, dr.mp, u, sm);   // p_j == q_j: draw from p_j
-  }
-  if (tid == 0) p.out_tokens[c * p.N + dr.n_acc] = tok;
 }
 
 inline int chunk_elems(int dtype) { return dtype == IDLM_BF16 ? kItemBytes / 2 : kItemBytes / 4; }
@@ -777,12 +1011,17 @@ size_t workspace_bytes(int C, int T, int V, int dtype, Params* p, void* base) {
   Partial* part = cv.take<Partial>(static_cast<size_t>(T) * CH);
   float* res_part = cv.take<float>(static_cast<size_t>(C) * CH);
   int32_t* res_cnt = cv.take<int32_t>(C);
-  Decision* dec = cv.take<Decision>(C);
+  PreRecord* pre = cv.take<PreRecord>(C);
+  const int nslice = (CH + kSliceChunks - 1) / kSliceChunks;
+  WorkItem* work = cv.take<WorkItem>(static_cast<size_t>(C) * std::max(nslice, 16));
+  int32_t* work_cnt = cv.take<int32_t>(1);
   if (p) {
     p->part = part;
     p->res_part = res_part;
     p->res_cnt = res_cnt;
-    p->dec = dec;
+    p->pre = pre;
+    p->work = work;
+    p->work_cnt = work_cnt;
   }
   return cv.used;
 }
@@ -796,8 +1035,17 @@ idlm_status launch(const Params& p, int dev, int sm_count, cudaStream_t stream) 
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= 64) return IDLM_ERR_CUDA;
     if (!done[dev]) {
+      // all three kernels ask for the largest shared-memory carveout, so that
+      // CTAs of kernels 2 and 3 may share an SM with a kernel-1 CTA
       if (cudaFuncSetAttribute(vocab_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kK1Smem)) != cudaSuccess)
+                               static_cast<int>(kK1Smem)) != cudaSuccess ||
+          cudaFuncSetAttribute(vocab_stream_kernel<T>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+          cudaFuncSetAttribute(decide_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+          cudaFuncSetAttribute(work_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return IDLM_ERR_CUDA;
       done[dev] = true;
     }
@@ -808,18 +1056,18 @@ idlm_status launch(const Params& p, int dev, int sm_count, cudaStream_t stream) 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return IDLM_ERR_CUDA;
 
-  // kernels 2 and 3 start early as programmatic dependents and wait in
-  // griddepcontrol.wait for the results of the kernel before them
+  // the decide and work kernels start early as programmatic dependents and
+  // wait in griddepcontrol.wait for the results of the kernel before them
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kK2Threads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(p.C);
+  cfg.blockDim = dim3(kDThreads);
   e = cudaLaunchKernelEx(&cfg, decide_kernel<T>, p);
   if (e != cudaSuccess) {
     // a stream that does not take programmatic serialisation: plain order
@@ -828,8 +1076,9 @@ idlm_status launch(const Params& p, int dev, int sm_count, cudaStream_t stream) 
     e = cudaLaunchKernelEx(&cfg, decide_kernel<T>, p);
   }
   if (e != cudaSuccess) return IDLM_ERR_CUDA;
-  cfg.gridDim = dim3(p.C * p.CH);
-  e = cudaLaunchKernelEx(&cfg, residual_kernel<T>, p);
+  cfg.gridDim = dim3(sm_count * kWorkPerSM);
+  cfg.blockDim = dim3(kWThreads);
+  e = cudaLaunchKernelEx(&cfg, work_kernel<T>, p);
   return cuda_status(e);
 }
 
@@ -898,6 +1147,7 @@ extern "C" idlm_status idlm_isd_accept(
   p.T = T;
   p.N = N;
   p.CH = CH;
+  p.nslice = (CH + acc::kSliceChunks - 1) / acc::kSliceChunks;
   p.chunk = acc::chunk_elems(dtype);
   p.greedy = temperature == 0.f;
   p.propose = proposal_mode;
