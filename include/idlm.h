@@ -130,6 +130,38 @@ idlm_status idlm_isd_attention(
     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * a3. Gated-LoRA projection (R-ISD).
+ *
+ * [IDLM] "Lossless R-ISD": a LoRA adapter is applied only at MASK positions;
+ * verify (clean) positions use the base weights alone, so their outputs equal
+ * the base model's bit for bit.  [IDLM] speedup panel: R-ISD overhead 1.12.
+ *
+ *   Y = X W^T + g_row * lora_scale * (X A^T) B^T,   g_row = row_gate[m] != 0
+ *
+ *   x          [M, K]  bf16   token rows of the step
+ *   w          [N, K]  bf16   base weight (row n gives output column n)
+ *   lora_a     [r, K]  bf16
+ *   lora_b     [N, r]  bf16
+ *   row_gate   [M]     uint8  1 at MASK rows, 0 at clean rows
+ *   y          [M, N]  bf16   written for every row
+ * fp32 accumulation on the tensor cores (tcgen05); the adapter enters the
+ * same accumulation as one more K step, so rows with row_gate = 0 come out
+ * bit-identical to the projection with lora_b = 0.  Requirements: K % 8 == 0,
+ * r % 8 == 0, 8 <= r <= 64, 16-byte aligned x, w, lora_a, lora_b; any M
+ * (token rows run in slices of 448).  Workspace:
+ * idlm_gated_lora_workspace_size(); its contents need no initialisation.
+ * The call launches two kernels per slice of 448 token rows (the adapter's
+ * X A^T product, then the GEMM as its programmatic dependent).  Device
+ * errors: TIMEOUT.
+ * ---------------------------------------------------------------------- */
+size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r);
+
+idlm_status idlm_gated_lora(
+    const void* x, const void* w, const void* lora_a, const void* lora_b,
+    const uint8_t* row_gate, float lora_scale, int M, int K, int N, int r, void* y,
+    void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * a4-a7. Accept: vocab pass, p/q acceptance, residual resample, bonus or
  * fresh draw, proposals and next state.
  *

@@ -60,6 +60,10 @@ def lib():
         L.idlm_isd_accept_noalloc.argtypes = (
             [vp, i32, i32] + [vp] * 5 + [i32, vp] + [i32, i32, i32, f32, i32, u64, u64]
             + [vp] * 10 + [vp, vp])
+        L.idlm_gated_lora_workspace_size.restype = sz
+        L.idlm_gated_lora_workspace_size.argtypes = [i32] * 4
+        L.idlm_gated_lora.restype = i32
+        L.idlm_gated_lora.argtypes = [vp] * 5 + [f32] + [i32] * 4 + [vp, vp, sz, vp, vp]
         L.idlm_kv_commit.restype = i32
         L.idlm_kv_commit.argtypes = ([vp, vp, vp, i32, vp, vp, vp, vp, vp, vp] + [i32] * 7
                                      + [vp, vp, vp])
@@ -168,6 +172,25 @@ def idlm_isd_accept_noalloc(logits, qo_indptr, mode, drafts, draft_q_stats, prev
         _ptr(next_q_stats), _ptr(next_mode), _ptr(next_mask_row0), _ptr(row_stats), _ptr(dbg),
         _ptr(status), _stream(stream))
     _check(rc, "idlm_isd_accept_noalloc")
+
+
+# ----------------------------------------------------------------- gated LoRA
+
+def idlm_gated_lora_workspace_size(M, K, N, r):
+    return int(lib().idlm_gated_lora_workspace_size(M, K, N, r))
+
+
+def idlm_gated_lora(x, w, lora_a, lora_b, row_gate, lora_scale, y, workspace, status,
+                    stream=None):
+    _contig(x, w, lora_a, lora_b, row_gate, y, workspace)
+    M, K = x.shape
+    N = w.shape[0]
+    r = lora_a.shape[0]
+    rc = lib().idlm_gated_lora(
+        _ptr(x), _ptr(w), _ptr(lora_a), _ptr(lora_b), _ptr(row_gate), float(lora_scale), M, K,
+        N, r, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _check(rc, "idlm_gated_lora")
 
 
 # --------------------------------------------------------------------- commit

@@ -1,0 +1,105 @@
+"""GPU parity of idlm_gated_lora (the tcgen05 gated-LoRA projection) against
+the oracle (marked gpu).
+
+Tolerance: outputs are stored in bf16 after fp32 accumulation, so they are
+compared with the attention bound, |gpu - oracle| <= 2e-2 + 1e-2 |oracle|,
+against the oracle's float64 result on the same bf16 inputs.  Rows whose gate
+is 0 must equal the same kernel's output without the adapter bit for bit
+("Lossless R-ISD": verify positions keep the base model's outputs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import speculative_verify_accept_step_b300 as lib
+from oracle import isd
+from speculative_verify_accept_step_b300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-2, 1e-2
+
+
+def f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def gpu_lora(x, w, a, b, g, s, dev="cuda"):
+    M, K = x.shape
+    N, r = w.shape[0], a.shape[0]
+    ws = torch.empty(lib.idlm_gated_lora_workspace_size(M, K, N, r), dtype=torch.uint8,
+                     device=dev)
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.idlm_gated_lora(x.to(dev), w.to(dev), a.to(dev), b.to(dev), g.to(dev), s, y, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    return y
+
+
+def case(M, K, N, r, seed, wstd=0.02):
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, K, generator=gen).bfloat16()
+    w = (torch.randn(N, K, generator=gen) * wstd).bfloat16()
+    a = (torch.randn(r, K, generator=gen) * wstd).bfloat16()
+    b = (torch.randn(N, r, generator=gen) * wstd).bfloat16()
+    g = (torch.arange(M) % 7 >= 4).to(torch.uint8)
+    return x, w, a, b, g
+
+
+def assert_close(got, ref):
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    worst = float((err / bound).max())
+    assert np.all(err <= bound), f"worst err/bound {worst:.3f}"
+    return worst
+
+
+@pytest.mark.parametrize("M,K,N,r", [(21, 136, 200, 16), (3, 64, 128, 8), (448, 512, 384, 16),
+                                     (600, 256, 256, 16), (130, 320, 520, 64)])
+def test_against_oracle_small(cuda_device, M, K, N, r):
+    x, w, a, b, g = case(M, K, N, r, seed=M + K + N)
+    y = gpu_lora(x, w, a, b, g, 1.0)
+    ref = isd.gated_lora(f64(x), f64(w), f64(a), f64(b), g.numpy(), 1.0)
+    assert_close(f64(y), ref)
+
+
+def test_lora_scale(cuda_device):
+    x, w, a, b, g = case(64, 256, 256, 16, seed=5, wstd=0.2)
+    y = gpu_lora(x, w, a, b, g, 0.5)
+    ref = isd.gated_lora(f64(x), f64(w), f64(a), f64(b), g.numpy(), 0.5)
+    assert_close(f64(y), ref)
+
+
+def test_ungated_rows_bit_identical_to_the_base_projection(cuda_device):
+    x, w, a, b, g = case(448, 1024, 512, 16, seed=7, wstd=0.2)
+    y = gpu_lora(x, w, a, b, g, 1.0)
+    y0 = gpu_lora(x, w, a, torch.zeros_like(b), g, 1.0)
+    clean = g == 0
+    assert torch.equal(y[clean.cuda()], y0[clean.cuda()])
+    # and the adapter does change the MASK rows
+    assert not torch.equal(y[~clean.cuda()], y0[~clean.cuda()])
+    # every gate off: the whole output equals the base projection
+    yoff = gpu_lora(x, w, a, b, torch.zeros_like(g), 1.0)
+    assert torch.equal(yoff, y0)
+
+
+@pytest.mark.parametrize("name", ["q", "k", "gate", "down"])
+def test_layer_projection_full_size_sampled(cuda_device, name):
+    """One projection of the workload's decoder layer (hidden 4096, FFN 12288,
+    448 token rows, rank 16) at full size, checked on 4096 sampled outputs
+    that the oracle computes one by one."""
+    w_ = wl.WORKLOADS["lora_layer_m448"]
+    inp = wl.lora_inputs(w_)
+    pj = inp["proj"][name]
+    x = inp["x"] if name != "down" else (torch.randn(448, w_.ffn, generator=torch.Generator().manual_seed(3))).bfloat16()
+    y = f64(gpu_lora(x, pj["w"], pj["a"], pj["b"], inp["row_gate"], inp["lora_scale"]))
+    M, N = y.shape
+    rng = np.random.default_rng(0)
+    ms, ns = rng.integers(0, M, 4096), rng.integers(0, N, 4096)
+    xs, ws_ = f64(x), None
+    wf, af, bf = f64(pj["w"]), f64(pj["a"]), f64(pj["b"])
+    g = inp["row_gate"].numpy()
+    ref = np.array([isd.gated_lora(xs[m:m + 1], wf[n:n + 1], af, bf[n:n + 1], g[m:m + 1],
+                                   inp["lora_scale"])[0, 0] for m, n in zip(ms, ns)])
+    assert_close(y[ms, ns], ref)
