@@ -55,8 +55,9 @@ def assert_close(got, ref):
     return worst
 
 
-@pytest.mark.parametrize("M,K,N,r", [(21, 136, 200, 16), (3, 64, 128, 8), (448, 512, 384, 16),
-                                     (600, 256, 256, 16), (130, 320, 520, 64)])
+@pytest.mark.parametrize("M,K,N,r", [(21, 136, 200, 16), (3, 64, 128, 8), (3, 64, 256, 8),
+                                     (448, 512, 384, 16), (600, 256, 256, 16), (130, 320, 520, 64),
+                                     (48, 4096, 128, 16)])
 def test_against_oracle_small(cuda_device, M, K, N, r):
     x, w, a, b, g = case(M, K, N, r, seed=M + K + N)
     y = gpu_lora(x, w, a, b, g, 1.0)
