@@ -41,6 +41,10 @@ def parse():
     ap.add_argument("--workload", default="isd_c64_n4_ctx4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-lora", action="store_true", help="skip the gated-LoRA leg")
+    ap.add_argument("--leg", default="step", choices=["step", "lora"],
+                    help="lora: only the gated-LoRA projections (prints their JSON)")
+    ap.add_argument("--lora-reps", type=int, default=20)
     ap.add_argument("--profile-run", action="store_true",
                     help="few launches for a profiler: no clock sampling, e2e or CPU leg")
     return ap.parse_args()
@@ -53,6 +57,49 @@ def peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     return 6400.0, 1800.0, "fallback"
+
+
+def lora_leg(dev, reps=20):
+    """The gated-LoRA projections of one decoder layer (workload lora_layer_m448:
+    hidden 4096, FFN 12288, 448 token rows, rank 16, gate on at MASK rows),
+    each through idlm_gated_lora, timed alone with CUDA events.  Returns
+    per-projection and whole-layer TFLOP/s (algorithmic 2 M K N per
+    projection; the adapter's extra work is not counted)."""
+    import speculative_verify_accept_step_b300 as L
+    from speculative_verify_accept_step_b300 import workloads as wl
+    w = wl.WORKLOADS["lora_layer_m448"]
+    inp = wl.lora_inputs(w)
+    x = inp["x"].to(dev)
+    xf = torch.randn(w.T, w.ffn, generator=torch.Generator().manual_seed(3)).bfloat16().to(dev)
+    gate = inp["row_gate"].to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, tot_flop, tot_ms = {}, 0.0, 0.0
+    for name in ("q", "k", "v", "o", "gate", "up", "down"):
+        pj = {k: v.to(dev) for k, v in inp["proj"][name].items()}
+        xi = xf if name == "down" else x
+        M, K = xi.shape
+        N, r = pj["w"].shape[0], pj["a"].shape[0]
+        ws = torch.empty(L.idlm_gated_lora_workspace_size(M, K, N, r), dtype=torch.uint8,
+                         device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            L.idlm_gated_lora(xi, pj["w"], pj["a"], pj["b"], gate, inp["lora_scale"], y, ws, st)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            L.idlm_gated_lora(xi, pj["w"], pj["a"], pj["b"], gate, inp["lora_scale"], y, ws, st)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        fl = 2.0 * M * K * N
+        tot_flop += fl
+        tot_ms += ms
+        out[name] = {"M": M, "K": K, "N": N, "us": ms * 1e3, "TFLOP/s": fl / ms / 1e9}
+        del ws, y
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    return {"workload": w.name, "projections": out, "layer_us": tot_ms * 1e3,
+            "TFLOP/s": tot_flop / tot_ms / 1e9, "launches_per_projection": 2}
 
 
 def source_hash(name):
@@ -313,6 +360,12 @@ def run_ours(args):
     both_gbs = (a_bytes + c_bytes) / ((att_ms + acc_ms) * 1e-3) / 1e9
 
     e2e = None if args.profile_run else run_e2e(st, args.e2e_steps, ws)
+    lora = None
+    if not args.profile_run and not args.no_lora:
+        lora = lora_leg(dev)
+        lora["peak"] = bf16
+        lora["frac"] = lora["TFLOP/s"] / bf16
+        lora["bound"] = "tensor"
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.profile_run:
         cpu = cpu_baseline(w, st.host)
@@ -352,10 +405,11 @@ def run_ours(args):
         "tokens_per_step": n_out / K,
         "accepted_drafts_per_step": n_acc / K,
         "accepted_drafts_per_s": allreduce(float(n_acc), ws, _sum_op()) / (ms * 1e-3),
-        "gpu_launches": 4 * K,
+        "gpu_launches": 5 * K,
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "lora": lora,
     }
     print(json.dumps(line))
 
@@ -524,6 +578,13 @@ def main():
     from speculative_verify_accept_step_b300.build import build
     if not os.path.exists(os.path.join(ROOT, "speculative_verify_accept_step_b300", "libidlm.so")):
         build()
+    if args.leg == "lora":
+        dev = torch.device("cuda", 0)
+        out = lora_leg(dev, reps=args.lora_reps)
+        _, bf16, kind = peaks()
+        out.update({"peak": bf16, "peak_kind": kind, "frac": out["TFLOP/s"] / bf16})
+        print(json.dumps(out))
+        return
     run_ours(args)
 
 
