@@ -298,6 +298,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
       if (ok) {
         const uint32_t kbase = smem_u32(stages + s * STAGE_BYTES);
         const uint32_t vbase = kbase + 2 * BOX_BYTES;
+        // S = Q K^T
         float sc[2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
@@ -311,53 +312,64 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
           mma_bf16_16816(sc[0], qa[ks], b0, b1);
           mma_bf16_16816(sc[1], qa[ks], b2, b3);
         }
-        // scale and mask: column key = 8n + qc + e
+        // mask keys past the request's context (cached pages) or past the
+        // row's own position (the step's new rows); a full cached page needs
+        // no mask.  Column key = 8n + qc + e.
         const int k = cur.k;
+        const bool full_page = k < nbc && (k + 1) * PS <= L;
+        if (!full_page) {
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
+          for (int n = 0; n < 2; ++n) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = 8 * n + qc + e;
-            bool ka, kb;
-            if (k < nbc) {
-              ka = kb = (k * PS + key) < L;
-            } else {
-              ka = key <= r_a;
-              kb = key <= r_b;
+            for (int e = 0; e < 2; ++e) {
+              const int key = 8 * n + qc + e;
+              bool ka, kb;
+              if (k < nbc) {
+                ka = kb = (k * PS + key) < L;
+              } else {
+                ka = key <= r_a;
+                kb = key <= r_b;
+              }
+              if (!ka) sc[n][e] = kNegInf;
+              if (!kb) sc[n][2 + e] = kNegInf;
             }
-            sc[n][e] = ka ? sc[n][e] * p.scale_log2 : kNegInf;
-            sc[n][2 + e] = kb ? sc[n][2 + e] * p.scale_log2 : kNegInf;
           }
         }
+        // online softmax in the log2 domain: p = 2^(s * scale - m)
         float mx_a = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
         float mx_b = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
         mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
         mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
         mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
         mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+        const float mn_a = fmaxf(m_a, mx_a * p.scale_log2), mn_b = fmaxf(m_b, mx_b * p.scale_log2);
         const float base_a = mn_a == kNegInf ? 0.f : mn_a;
         const float base_b = mn_b == kNegInf ? 0.f : mn_b;
-        const float corr_a = fast_exp2(m_a - base_a), corr_b = fast_exp2(m_b - base_b);
-        m_a = mn_a;
-        m_b = mn_b;
+        // rescale O only when some row's maximum rose (otherwise the factor is 1)
+        if (__any_sync(0xffffffffu, mn_a != m_a || mn_b != m_b)) {
+          const float corr_a = fast_exp2(m_a - base_a), corr_b = fast_exp2(m_b - base_b);
+          l_a *= corr_a;
+          l_b *= corr_b;
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            o[n][0] *= corr_a;
+            o[n][1] *= corr_a;
+            o[n][2] *= corr_b;
+            o[n][3] *= corr_b;
+          }
+          m_a = mn_a;
+          m_b = mn_b;
+        }
         float pr[2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
-          pr[n][0] = fast_exp2(sc[n][0] - base_a);
-          pr[n][1] = fast_exp2(sc[n][1] - base_a);
-          pr[n][2] = fast_exp2(sc[n][2] - base_b);
-          pr[n][3] = fast_exp2(sc[n][3] - base_b);
+          pr[n][0] = fast_exp2(fmaf(sc[n][0], p.scale_log2, -base_a));
+          pr[n][1] = fast_exp2(fmaf(sc[n][1], p.scale_log2, -base_a));
+          pr[n][2] = fast_exp2(fmaf(sc[n][2], p.scale_log2, -base_b));
+          pr[n][3] = fast_exp2(fmaf(sc[n][3], p.scale_log2, -base_b));
         }
-        l_a = l_a * corr_a + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-        l_b = l_b * corr_b + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          o[n][0] *= corr_a;
-          o[n][1] *= corr_a;
-          o[n][2] *= corr_b;
-          o[n][3] *= corr_b;
-        }
+        l_a += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+        l_b += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
         uint32_t pa[4];
         pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
         pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
