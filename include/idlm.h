@@ -149,10 +149,17 @@ idlm_status idlm_isd_attention(
  * bit-identical to the projection with lora_b = 0.  Requirements: K % 8 == 0,
  * r % 8 == 0, 8 <= r <= 64, 16-byte aligned x, w, lora_a, lora_b; any M
  * (token rows run in slices of 448).  Workspace:
- * idlm_gated_lora_workspace_size(); its contents need no initialisation.
+ * idlm_gated_lora_workspace_size() bytes, 256-byte aligned (the adapter
+ * operands, and fp32 partial tiles with one flag per SM for the split of the
+ * K sum); its contents need no initialisation, and one workspace must not be
+ * used by two calls at once.  The size depends on the current device.
  * The call launches two kernels per slice of 448 token rows (the adapter's
- * X A^T product, then the GEMM as its programmatic dependent).  Device
- * errors: TIMEOUT.
+ * X A^T product, then the GEMM as its programmatic dependent).  The GEMM is
+ * a persistent grid of at most one CTA per SM that splits the (tile, K
+ * step) work evenly; where a tile's K sum is split, its partial sums are
+ * added in a fixed order, so results are reproducible on a given device.
+ * The environment variable IDLM_LORA_GRID, if set, fixes the grid size
+ * (capped at the SMs).  Device errors: TIMEOUT.
  * ---------------------------------------------------------------------- */
 size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r);
 

@@ -59,7 +59,8 @@ bool encode_bf16_map(CUtensorMap* map, void* base, int rank, const uint64_t* dim
   }
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, gdim, gstride, bdim, estride,
                    CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   swizzle_bytes == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                   swizzle_bytes == 0    ? CU_TENSOR_MAP_SWIZZLE_NONE
+                   : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                    : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                          : CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

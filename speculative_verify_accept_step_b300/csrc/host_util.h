@@ -25,7 +25,8 @@ bool current_device_info(DeviceInfo* out);
 // cuTensorMapEncodeTiled, resolved once from the driver.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
-// Encode a tiled bf16 tensor map with a 128-, 64- or 32-byte swizzle.
+// Encode a tiled bf16 tensor map with a 128-, 64- or 32-byte swizzle, or
+// none (swizzle_bytes = 0).
 // dims/strides are innermost first; strides (bytes) exclude dimension 0.
 bool encode_bf16_map(CUtensorMap* map, void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes = 128);

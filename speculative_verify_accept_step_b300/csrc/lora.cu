@@ -22,20 +22,32 @@
 // adapter.
 //
 // Kernels:
-//   lora_t_kernel     T = g s X A^T in fp32 on CUDA cores, stored as bf16
-//                     (a [M x r] product, 0.03% of the flops), and B padded
-//                     to 64 columns.
+//   lora_t_kernel     T = g s X A^T with mma.sync (fp32 accumulation, K
+//                     split over CTAs, summed in a fixed order), stored as
+//                     bf16 (a [M x r] product, 0.03% of the flops), and B
+//                     padded to 64 columns.
 //   lora_gemm_kernel  tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in
 //                     TMEM), operands staged by TMA (cp.async.bulk.tensor,
-//                     128-byte swizzle) in a 3-stage ring.  Warp 0 issues
-//                     the loads, warp 1 owns TMEM and issues the MMAs (one
-//                     thread), warps 2-5 drain TMEM with tcgen05.ld and
+//                     128-byte swizzle) in a ring of up to 8 stages.  Warp 0
+//                     issues the loads, warp 1 owns TMEM and issues the MMAs
+//                     (one thread), warps 2-5 drain TMEM with tcgen05.ld and
 //                     write Y.  A programmatic dependent of lora_t_kernel:
-//                     only the load of T waits for it.
+//                     only the adapter step waits for it.
+// The GEMM is a persistent stream-K grid of at most one CTA per SM: the
+// (tile, K step) units are cut into equal ranges, so projections with few
+// weight tiles (N / 128 well below the 148 SMs) still fill the GPU.  A tile
+// cut by a range boundary is summed from fp32 partial tiles in CTA order by
+// the CTA holding its first K step, so results do not depend on timing.  The
+// host picks the grid from a cost model of K steps and epilogue costs.  The
+// last segment of a CTA's range writes its Y tile from the idle ring by TMA
+// store.
 // Every mbarrier wait is bounded; a wait that runs out records
 // IDLM_DEV_TIMEOUT, and the CTA drains its copies and MMAs and frees its
 // tensor memory before it leaves.
 #include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -46,23 +58,83 @@ namespace lora {
 
 constexpr int kBK = 64;                    // K values per stage (128 bytes of bf16)
 constexpr int kTileN = 128;                // weight rows per tile (MMA M)
-constexpr int kStages = 3;
-constexpr int kMaxTokens = 448;            // tokens per launch: TMEM columns (<= 512) and a
-                                           // 3-stage ring of 72 KB stages
+constexpr int kMaxStages = 8;
+constexpr int kMaxTokens = 448;            // tokens per launch: TMEM columns (<= 512) and
+                                           // three 72 KB stages
 constexpr int kThreads = 192;              // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr uint32_t kTmemCols = 512;        // allocation: a power of two >= the tokens
+constexpr uint32_t kAccCols = 256;         // one of two accumulators when m16 <= 256
 constexpr uint32_t kWBytes = kTileN * kBK * 2;   // 16 KB
+constexpr uint32_t kStageY = 16 * kTileN * 2;    // Y staging: 16 tokens x 128 columns, bf16
+constexpr int kEpiBar = 1;                 // named barrier of the four epilogue warps
+constexpr int kMaxPSlots = 12;             // partial-tile pieces in flight (16 KB each)
+constexpr uint32_t kPiece = 16384;         // one piece: 32 tokens x 128 rows, fp32
+constexpr uint32_t kBarBytes = 512;
+constexpr int kYBoxRows = 16;              // token rows per TMA store of Y
 
 struct Params {
   __nv_bfloat16* y;
-  const uint8_t* row_gate;
+  float* part;              // [G][m16 / 4][128][4] fp32 partial tiles, one slot per CTA
+  unsigned long long* flag; // [G] = epoch once the CTA's partial tile is written
+  unsigned long long epoch; // distinct for every launch
   int32_t* status;
-  int M, K, N, r;
+  int M, N, r;
   int m16;        // tokens rounded up to 16
   int n1, n2;     // MMA N of the two token blocks (n1 <= 256, n2 = m16 - n1)
   int tiles, kb;  // weight-row tiles, K blocks
-  uint32_t stage_bytes;
+  int S;          // K steps of a tile: kb K blocks, then the adapter step
+  long long U;    // tiles * S units of work, split evenly over the grid
+  int stages;     // depth of the stage ring
+  int nacc;       // accumulators in TMEM (2 when m16 <= 256)
+  int yvec;       // Y rows allow 16-byte stores (N % 8 == 0, aligned base)
+  int pslots;     // 16 KB slots of the ring that stage partial tiles for the finaliser
+  int ytma;       // the last segment's Y tile goes out by TMA store from the ring
+  uint32_t ytile_off;   // ring offset of that [m16 x 128] bf16 tile
+  uint32_t stage_bytes;   // one stage: the weight block, then the token rows
 };
+
+// Stream-K split of the work: the units (tile, k) in tile-major order are
+// cut into gridDim.x equal ranges, one per CTA.  A range is walked as
+// segments (its units within one tile).  Only the first segment of a range
+// can start inside a tile (k0 > 0): such a segment is a partial tile, stored
+// in fp32 in the CTA's workspace slot.  The CTA whose range holds (tile, 0)
+// and not the whole tile finalises it: it adds the partials of the next
+// CTAs (in CTA order) to its own accumulator and writes Y.  The partials
+// come from the beginnings of those CTAs' ranges, so they are ready long
+// before the finaliser, which reaches the tile at the end of its range.
+struct Seg {
+  int tile, k0, k1;
+};
+__device__ __forceinline__ long long range_begin(const Params& p, int c) {
+  return static_cast<long long>(c) * p.U / gridDim.x;
+}
+__device__ __forceinline__ Seg seg_at(const Params& p, long long pos, long long end) {
+  Seg s;
+  s.tile = static_cast<int>(pos / p.S);
+  s.k0 = static_cast<int>(pos - static_cast<long long>(s.tile) * p.S);
+  s.k1 = static_cast<int>(min(static_cast<long long>(p.S), end - static_cast<long long>(s.tile) * p.S));
+  return s;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// TMA store of a [rows x 128] bf16 box from shared memory (no swizzle).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory");
+}
 
 // ------------------------------------------------------------- tcgen05 PTX
 
@@ -123,6 +195,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Issue a load of 32 TMEM columns into r without waiting; r must not be
+// read before tmem_ld_wait(r).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+// Wait for this thread's TMEM loads; r is tied to the wait so that no read
+// of it moves above it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
 // and B, both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
@@ -148,133 +248,215 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
 
 // ------------------------------------------------------------------ T = g s X A^T
 //
-// The first ceil(M / 4) CTAs: one CTA per 4 token rows; each thread
-// accumulates the 4 x r partial dots of its K-slice, then the block sums
-// them.  Rows with g = 0 get zeros.  T is stored [M x 64] (zeros past r).
-// The remaining CTAs copy B [N x r] to B64 [N x 64] (zeros past r), so that
-// both operands of the LoRA step are plain 128-byte rows for TMA.
-constexpr int kTRows = 4;
-constexpr int kTThreads = 256;
-constexpr int kPadW = 64;   // padded LoRA rank
+// Grid: (row groups of 16 tokens) x (K slices of 512), then the CTAs that
+// pad B.  A CTA's 4 warps take 128 K values each of its slice and
+// accumulate the [16 x r] product X A^T with mma.sync (m16n8k16, bf16 in,
+// fp32 accumulate); the CTA adds its warps' sums in warp order and stores
+// the slice's fp32 partial.  The last CTA of a row group to finish (a
+// counter tagged with the launch's epoch, so the workspace needs no
+// clearing) adds the slices in slice order and stores T = g s (X A^T) in
+// bf16, [M x 64] with zeros past r and at rows with g = 0.  The padding CTAs
+// copy B [N x r] to B64 [N x 64] (zeros past r), so that both operands of
+// the LoRA step are plain 128-byte rows for TMA.  2 KB of shared memory, so
+// that these CTAs fit beside a GEMM CTA on one SM.
+constexpr int kTRows = 16;
+constexpr int kTThreads = 128;
+constexpr int kTWarps = kTThreads / 32;
+constexpr int kTSlice = 512;   // K values per CTA
+constexpr int kPadW = 64;      // padded LoRA rank
 
-__global__ void __launch_bounds__(kTThreads) lora_t_kernel(const __nv_bfloat16* x,
-                                                           const __nv_bfloat16* a,
-                                                           const __nv_bfloat16* b,
-                                                           const uint8_t* gate, float scale,
-                                                           int M, int K, int N, int r,
-                                                           __nv_bfloat16* t64,
-                                                           __nv_bfloat16* b64) {
-  __shared__ float red[kTThreads / 32][kTRows][16];
+__device__ __forceinline__ uint32_t ldg32(const __nv_bfloat16* p) {
+  return __ldg(reinterpret_cast<const unsigned int*>(p));
+}
+
+struct TParams {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* a;
+  const __nv_bfloat16* b;
+  const uint8_t* gate;
+  float scale;
+  int M, K, N, r;
+  int kslices;                  // ceil(K / kTSlice)
+  float* tpart;                 // [kslices][ceil(M / 16) * 16][kPadW] fp32
+  unsigned long long* tcount;   // [ceil(M / 16)]: epoch << 32 | slices done
+  unsigned long long epoch;
+  __nv_bfloat16* t64;
+  __nv_bfloat16* b64;
+};
+
+__global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
+  __shared__ float red[kTWarps][kTRows][8];
+  __shared__ int last;
   griddep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tblocks = (M + kTRows - 1) / kTRows;
+  const int groups = (p.M + kTRows - 1) / kTRows;
+  const int tblocks = groups * p.kslices;
   if (static_cast<int>(blockIdx.x) >= tblocks) {
     const int n = (blockIdx.x - tblocks) * kTThreads + tid;
-    if (n < N)
-      for (int j = 0; j < kPadW; ++j)
-        b64[static_cast<size_t>(n) * kPadW + j] =
-            j < r ? b[static_cast<size_t>(n) * r + j] : __float2bfloat16_rn(0.f);
+    if (n < p.N) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.b + static_cast<size_t>(n) * p.r);
+      uint4* dst = reinterpret_cast<uint4*>(p.b64 + static_cast<size_t>(n) * kPadW);
+#pragma unroll
+      for (int q = 0; q < kPadW / 8; ++q)
+        dst[q] = q < p.r / 8 ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+    }
     return;
   }
-  const int m0 = blockIdx.x * kTRows;
-  // zero the padding and the ungated rows
-  for (int e = tid; e < kTRows * kPadW; e += kTThreads) {
-    const int i = e / kPadW, j = e % kPadW;
-    if (m0 + i < M && (j >= r || !gate[m0 + i]))
-      t64[static_cast<size_t>(m0 + i) * kPadW + j] = __float2bfloat16_rn(0.f);
+  const int grp = blockIdx.x / p.kslices, ks = blockIdx.x % p.kslices;
+  const int m0 = grp * kTRows;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int nt = p.r / 8;
+  float acc[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+  const bool r0 = m0 + g < p.M, r1 = m0 + g + 8 < p.M;
+  const __nv_bfloat16* x0 = p.x + static_cast<size_t>(r0 ? m0 + g : 0) * p.K;
+  const __nv_bfloat16* x1 = p.x + static_cast<size_t>(r1 ? m0 + g + 8 : 0) * p.K;
+  const int kw = ks * kTSlice + warp * (kTSlice / kTWarps);
+#pragma unroll
+  for (int st = 0; st < kTSlice / kTWarps / 16; ++st) {
+    const int k = kw + st * 16 + 2 * t4;
+    const bool lo = k < p.K, hi = k + 8 < p.K;   // K % 8 == 0: pairs never straddle K
+    uint32_t af[4];
+    af[0] = (r0 && lo) ? ldg32(x0 + k) : 0u;
+    af[1] = (r1 && lo) ? ldg32(x1 + k) : 0u;
+    af[2] = (r0 && hi) ? ldg32(x0 + k + 8) : 0u;
+    af[3] = (r1 && hi) ? ldg32(x1 + k + 8) : 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nt) {
+        const __nv_bfloat16* ar = p.a + static_cast<size_t>(j * 8 + g) * p.K;
+        mma_bf16_16816(acc[j], af, lo ? ldg32(ar + k) : 0u, hi ? ldg32(ar + k + 8) : 0u);
+      }
   }
-  bool any = false;
-  for (int i = 0; i < kTRows; ++i) any |= (m0 + i < M) && gate[m0 + i];
-  if (!any) return;
-  for (int j0 = 0; j0 < r; j0 += 16) {
-    const int nj = min(16, r - j0);
-    float acc[kTRows][16];
+  // this slice's sum over its warps, in warp order
+  float* mine = p.tpart + (static_cast<size_t>(ks) * groups * kTRows + m0) * kPadW;
 #pragma unroll
-    for (int i = 0; i < kTRows; ++i)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) acc[i][j] = 0.f;
-    for (int k = tid * 8; k < K; k += kTThreads * 8) {
-      float xv[kTRows][8];
-#pragma unroll
-      for (int i = 0; i < kTRows; ++i) {
-        if (m0 + i < M) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(m0 + i) * K + k));
-          xv[i][0] = bf16_lo(w.x); xv[i][1] = bf16_hi(w.x);
-          xv[i][2] = bf16_lo(w.y); xv[i][3] = bf16_hi(w.y);
-          xv[i][4] = bf16_lo(w.z); xv[i][5] = bf16_hi(w.z);
-          xv[i][6] = bf16_lo(w.w); xv[i][7] = bf16_hi(w.w);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) xv[i][e] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (j < nj) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(a + static_cast<size_t>(j0 + j) * K + k));
-          const float av[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                               bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-#pragma unroll
-          for (int i = 0; i < kTRows; ++i)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[i][j] = fmaf(xv[i][e], av[e], acc[i][j]);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kTRows; ++i)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float v = acc[i][j];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[warp][i][j] = v;
-      }
+  for (int j = 0; j < 8; ++j) {
+    if (j >= nt) break;
+    red[warp][g][2 * t4] = acc[j][0];
+    red[warp][g][2 * t4 + 1] = acc[j][1];
+    red[warp][g + 8][2 * t4] = acc[j][2];
+    red[warp][g + 8][2 * t4 + 1] = acc[j][3];
     __syncthreads();
-    if (tid < kTRows * 16) {
-      const int i = tid / 16, j = tid % 16;
-      if (j < nj && m0 + i < M && gate[m0 + i]) {
-        float v = 0.f;
-        for (int w = 0; w < kTThreads / 32; ++w) v += red[w][i][j];
-        t64[static_cast<size_t>(m0 + i) * kPadW + j0 + j] = __float2bfloat16_rn(v * scale);
-      }
+    {
+      const int i = tid / 8, c = tid % 8;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kTWarps; ++w) v += red[w][i][c];
+      __stcg(mine + i * kPadW + j * 8 + c, v);
     }
     __syncthreads();
+  }
+  // the last slice of the row group to finish adds the slices in order
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned long long tag = (p.epoch & 0xffffffffull) << 32;
+    unsigned long long* cnt = p.tcount + grp;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt), seen;
+    do {
+      seen = old;
+      const unsigned long long nv = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
+      old = atomicCAS(cnt, seen, nv);
+    } while (old != seen);
+    const unsigned long long now = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
+    last = (now & 0xffffffffull) == static_cast<unsigned long long>(p.kslices);
+    __threadfence();
+  }
+  __syncthreads();
+  if (!last) return;
+  // the r columns: slices added in slice order, 8 loads in flight at a time
+  for (int e = tid; e < kTRows * p.r; e += kTThreads) {
+    const int i = e / p.r, c = e % p.r, m = m0 + i;
+    if (m >= p.M) continue;
+    float v = 0.f;
+    if (p.gate[m]) {
+      const float* src = p.tpart + static_cast<size_t>(m) * kPadW + c;
+      const size_t stride = static_cast<size_t>(groups) * kTRows * kPadW;
+      for (int s0 = 0; s0 < p.kslices; s0 += 8) {
+        float u[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) u[q] = s0 + q < p.kslices ? __ldcg(src + (s0 + q) * stride) : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (s0 + q < p.kslices) v += u[q];
+      }
+      v *= p.scale;
+    }
+    p.t64[static_cast<size_t>(m) * kPadW + c] = __float2bfloat16_rn(v);
+  }
+  for (int e = tid; e < kTRows * (kPadW - p.r); e += kTThreads) {
+    const int i = e / (kPadW - p.r), c = p.r + e % (kPadW - p.r), m = m0 + i;
+    if (m < p.M) p.t64[static_cast<size_t>(m) * kPadW + c] = __float2bfloat16_rn(0.f);
   }
 }
 
 // ------------------------------------------------------------ the GEMM
 
-// Dynamic shared memory: the stage ring (1024-byte aligned), then barriers.
-__host__ __device__ inline size_t bar_offset(uint32_t stage_bytes) {
-  return size_t(kStages) * stage_bytes;
+// Dynamic shared memory: the stage ring (1024-byte aligned), the Y staging
+// tile, then the barriers.
+__host__ __device__ inline size_t stage_y_offset(int stages, uint32_t stage_bytes) {
+  return size_t(stages) * stage_bytes;
 }
-inline size_t smem_bytes(uint32_t stage_bytes) { return 1024 + bar_offset(stage_bytes) + 256; }
+__host__ __device__ inline size_t bar_offset(int stages, uint32_t stage_bytes) {
+  return stage_y_offset(stages, stage_bytes) + kStageY;
+}
+inline size_t smem_bytes(int stages, uint32_t stage_bytes) {
+  return 1024 + bar_offset(stages, stage_bytes) + kBarBytes;
+}
+
+// Spin (bounded) until *f == v with acquire semantics.
+__device__ bool wait_flag(const unsigned long long* f, unsigned long long v, int32_t* status) {
+  if (ld_acquire_u64(f) == v) return true;
+  const unsigned long long t0 = globaltimer();
+  while (ld_acquire_u64(f) != v) {
+    if (globaltimer() - t0 > kWaitNs) {
+      set_status(status, IDLM_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map1,
                  const __grid_constant__ CUtensorMap x_map2, const __grid_constant__ CUtensorMap b_map,
                  const __grid_constant__ CUtensorMap t_map1, const __grid_constant__ CUtensorMap t_map2,
-                 const Params p) {
+                 const __grid_constant__ CUtensorMap y_map, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + bar_offset(p.stage_bytes));
-  uint64_t* full = bars;                    // [kStages] TMA -> MMA
-  uint64_t* empty = bars + kStages;         // [kStages] MMA -> TMA
-  uint64_t* tmem_full = bars + 2 * kStages; // MMA -> epilogue
-  uint64_t* tmem_empty = tmem_full + 1;     // epilogue -> MMA
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(tmem_empty + 1);
+  __nv_bfloat16* ystage =
+      reinterpret_cast<__nv_bfloat16*>(base + stage_y_offset(p.stages, p.stage_bytes));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + bar_offset(p.stages, p.stage_bytes));
+  uint64_t* full = bars;                        // [stages] TMA -> MMA
+  uint64_t* empty = bars + kMaxStages;          // [stages] MMA -> TMA
+  uint64_t* tmem_full = bars + 2 * kMaxStages;  // [2] MMA -> epilogue
+  uint64_t* tmem_empty = tmem_full + 2;         // [2] epilogue -> MMA
+  uint64_t* drain = tmem_empty + 2;             // MMA issuer, after an abort
+  uint64_t* pbar = drain + 1;                   // [kMaxPSlots] partial pieces -> finaliser
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(pbar + kMaxPSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base + 1);
+  volatile int* epi_fail = abort_flag + 1;      // set by an epilogue warp, read after epi_sync
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long r_begin = range_begin(p, blockIdx.x), r_end = range_begin(p, blockIdx.x + 1);
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 4);   // one arrival per epilogue warp
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 4);   // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    for (int i = 0; i < kMaxPSlots; ++i) mbar_init(&pbar[i], 1);
     *abort_flag = 0;
+    *epi_fail = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -285,66 +467,77 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base;
-  const int nsteps = p.kb + 1;   // K blocks, then the LoRA block
 
+  // The producer and MMA warps run their loops with all 32 lanes (the waits
+  // are warp-uniform); lane 0 issues the copies and the MMAs.
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&w_map);
       prefetch_tensormap(&x_map1);
       prefetch_tensormap(&x_map2);
-      int issued = 0;
-      bool ok = true;
-      bool t_ready = false;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-        for (int k = 0; k < nsteps; ++k, ++issued) {
-          const int s = issued % kStages;
-          const uint32_t ph = (issued / kStages) & 1;
-          if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          uint8_t* st = base + size_t(s) * p.stage_bytes;
-          mbar_arrive_expect_tx(&full[s], p.stage_bytes);
-          if (k < p.kb) {
-            tma_load_2d(st, &w_map, &full[s], k * kBK, tile * kTileN);
-            tma_load_2d(st + kWBytes, &x_map1, &full[s], k * kBK, 0);
-            if (p.n2) tma_load_2d(st + kWBytes + p.n1 * 128, &x_map2, &full[s], k * kBK, p.n1);
-          } else {
-            if (!t_ready) {   // T comes from lora_t_kernel
-              griddep_wait();
-              t_ready = true;
-            }
-            tma_load_2d(st, &b_map, &full[s], 0, tile * kTileN);
-            tma_load_2d(st + kWBytes, &t_map1, &full[s], 0, 0);
-            if (p.n2) tma_load_2d(st + kWBytes + p.n1 * 128, &t_map2, &full[s], 0, p.n1);
-          }
-        }
-      }
-      // every issued copy lands before the CTA may leave
-      for (int i = max(0, issued - kStages); i < issued; ++i)
-        mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, nullptr, p.status);
     }
+    const uint32_t tx = kWBytes + static_cast<uint32_t>(p.m16) * 128;
+    int issued = 0;
+    bool ok = true;
+    bool t_ready = false;
+    for (long long pos = r_begin; ok && pos < r_end;) {
+      const Seg sg = seg_at(p, pos, r_end);
+      for (int k = sg.k0; k < sg.k1; ++k, ++issued) {
+        const int s = issued % p.stages;
+        const uint32_t ph = (issued / p.stages) & 1;
+        if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const bool lora_step = k == p.kb;   // B and T, written by lora_t_kernel
+        if (lora_step && !t_ready) {
+          griddep_wait();
+          t_ready = true;
+        }
+        if (lane == 0) {
+          uint8_t* st = base + size_t(s) * p.stage_bytes;
+          const CUtensorMap* am = lora_step ? &b_map : &w_map;
+          const CUtensorMap* bm1 = lora_step ? &t_map1 : &x_map1;
+          const CUtensorMap* bm2 = lora_step ? &t_map2 : &x_map2;
+          const int kx = lora_step ? 0 : k * kBK;
+          mbar_arrive_expect_tx(&full[s], tx);
+          tma_load_2d(st, am, &full[s], kx, sg.tile * kTileN);
+          tma_load_2d(st + kWBytes, bm1, &full[s], kx, 0);
+          if (p.n2) tma_load_2d(st + kWBytes + p.n1 * 128, bm2, &full[s], kx, p.n1);
+        }
+        __syncwarp();
+      }
+      pos = static_cast<long long>(sg.tile) * p.S + sg.k1;
+    }
+    // every copy into the ring lands before the CTA may leave
+    for (int i = max(0, issued - p.stages); i < issued; ++i)
+      mbar_wait_bounded(&full[i % p.stages], (i / p.stages) & 1, nullptr, p.status);
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc1 = make_idesc(kTileN, p.n1);
-      const uint32_t idesc2 = make_idesc(kTileN, p.n2 ? p.n2 : 16);
-      const int ksub_lora = (p.r + 15) / 16;
-      int consumed = 0, t_iter = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++t_iter) {
-        // the epilogue has drained the previous tile's accumulator
-        if (!mbar_wait_bounded(tmem_empty, (t_iter & 1) ^ 1, abort_flag, p.status)) break;
+    const uint32_t idesc1 = make_idesc(kTileN, p.n1);
+    const uint32_t idesc2 = make_idesc(kTileN, p.n2 ? p.n2 : 16);
+    const int ksub_lora = (p.r + 15) / 16;
+    int consumed = 0, t_iter = 0;
+    bool ok = true;
+    for (long long pos = r_begin; ok && pos < r_end; ++t_iter) {
+      const Seg sg = seg_at(p, pos, r_end);
+      pos = static_cast<long long>(sg.tile) * p.S + sg.k1;
+      const int a = t_iter % p.nacc;
+      const uint32_t use = t_iter / p.nacc;
+      // the epilogue has drained this accumulator's previous segment
+      if (!mbar_wait_bounded(&tmem_empty[a], (use & 1) ^ 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t d = tmem + a * kAccCols;
+      for (int k = sg.k0; k < sg.k1; ++k, ++consumed) {
+        const int s = consumed % p.stages;
+        const uint32_t ph = (consumed / p.stages) & 1;
+        if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        for (int k = 0; k < nsteps; ++k, ++consumed) {
-          const int s = consumed % kStages;
-          const uint32_t ph = (consumed / kStages) & 1;
-          if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (lane == 0) {
           const uint32_t sa = smem_u32(base + size_t(s) * p.stage_bytes);
           const uint64_t a_desc = make_sdesc(sa);
           const uint64_t b1_desc = make_sdesc(sa + kWBytes);
@@ -353,42 +546,203 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
           for (int j = 0; j < nsub; ++j) {
             // advance 16 values (32 bytes) along K inside the swizzled rows
             const uint64_t off = static_cast<uint64_t>(j * 2);
-            const uint32_t acc = (k > 0 || j > 0) ? 1u : 0u;
-            mma_bf16(tmem, a_desc + off, b1_desc + off, idesc1, acc);
-            if (p.n2) mma_bf16(tmem + p.n1, a_desc + off, b2_desc + off, idesc2, acc);
+            const uint32_t acc = (k > sg.k0 || j > 0) ? 1u : 0u;
+            mma_bf16(d, a_desc + off, b1_desc + off, idesc1, acc);
+            if (p.n2) mma_bf16(d + p.n1, a_desc + off, b2_desc + off, idesc2, acc);
           }
           mma_commit(&empty[s]);   // the stage is free once these MMAs finish
         }
-        mma_commit(tmem_full);     // the tile's accumulator is complete
+        __syncwarp();
       }
-      // no MMA may still run when the tensor memory is freed
-      if (*abort_flag) {
-        mma_commit(tmem_full);
-        mbar_wait_bounded(tmem_full, t_iter & 1, nullptr, p.status);
-      }
+      if (ok && lane == 0) mma_commit(&tmem_full[a]);   // the segment's accumulator is complete
+      __syncwarp();
+    }
+    // no MMA may still run when the tensor memory is freed
+    if (*abort_flag) {
+      if (lane == 0) mma_commit(drain);
+      __syncwarp();
+      mbar_wait_bounded(drain, 0, nullptr, p.status);
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    // Thread `row` (0..127) owns weight row tile * 128 + row: TMEM lane row.
+    // Every decision that ends the loop is taken after epi_sync, from
+    // shared state, so the four warps always meet the same barriers.  The
+    // next 32 TMEM columns load while the current ones are written out.
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int et = tid - 64;   // 0..127
+    const int nq = p.m16 / 4;  // float4 groups of a partial tile row
+    const float4* part4 = reinterpret_cast<const float4*>(p.part);
     int t_iter = 0;
-    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++t_iter) {
-      if (!mbar_wait_bounded(tmem_full, t_iter & 1, abort_flag, p.status)) break;
+    for (long long pos = r_begin; pos < r_end; ++t_iter) {
+      const Seg sg = seg_at(p, pos, r_end);
+      pos = static_cast<long long>(sg.tile) * p.S + sg.k1;
+      const int a = t_iter % p.nacc;
+      const uint32_t use = t_iter / p.nacc;
+      if (!mbar_wait_bounded(&tmem_full[a], use & 1, nullptr, p.status)) {
+        *epi_fail = 1;
+        *abort_flag = 1;
+      }
+      epi_sync();
+      if (*epi_fail) break;
       tc_fence_after();
-      const int n = tile * kTileN + q * 32 + lane;   // weight row = output column
-      for (int c0 = 0; c0 < p.m16; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
-        if (n < p.N) {
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * kAccCols;
+      uint32_t ra[32], rb[32];
+      tmem_ld32_async(taddr, ra);
+      tmem_ld_wait(ra);
+      if (sg.k0 > 0) {
+        // a partial tile: into this CTA's workspace slot, then the flag
+        float4* dst = reinterpret_cast<float4*>(p.part) + static_cast<size_t>(blockIdx.x) * nq * kTileN;
+        for (int c0 = 0; c0 < p.m16; c0 += 32) {
+          const bool more = c0 + 32 < p.m16;
+          if (more) tmem_ld32_async(taddr + c0 + 32, rb);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = c0 + j;
-            if (m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(v[j]);
+          for (int g = 0; g < 8; ++g)
+            if (c0 + 4 * g < p.m16)
+              __stcg(dst + static_cast<size_t>(c0 / 4 + g) * kTileN + row,
+                     make_float4(__uint_as_float(ra[4 * g]), __uint_as_float(ra[4 * g + 1]),
+                                 __uint_as_float(ra[4 * g + 2]), __uint_as_float(ra[4 * g + 3])));
+          if (more) {
+            tmem_ld_wait(rb);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ra[j] = rb[j];
           }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[a]);
+        __threadfence();
+        epi_sync();
+        if (et == 0) st_release_u64(&p.flag[blockIdx.x], p.epoch);
+        continue;
+      }
+      // A whole tile, or the head of a tile whose other segments are the
+      // partials of the next CTAs.  Those arrive in 16 KB pieces (32 tokens
+      // of one partial) by bulk copy into the ring, which is idle now: the
+      // head is the last segment of this CTA's range.
+      int c_lo = blockIdx.x + 1, c_hi = c_lo;
+      if (sg.k1 < p.S) {
+        const long long tile_end = static_cast<long long>(sg.tile + 1) * p.S;
+        while (c_hi < static_cast<int>(gridDim.x) && range_begin(p, c_hi) < tile_end) ++c_hi;
+        if (et == 0) {
+          for (int c = c_lo; c < c_hi; ++c)
+            if (!wait_flag(&p.flag[c], p.epoch, p.status)) {
+              *epi_fail = 1;
+              *abort_flag = 1;
+              break;
+            }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        epi_sync();
+        if (*epi_fail) break;
+      }
+      const int ncon = c_hi - c_lo;
+      const int npieces = ((p.m16 + 31) / 32) * ncon;
+      int issued = 0;
+      // issue pieces [issued, upto) into their slots
+      auto issue = [&](int upto) {
+        for (; issued < upto && issued < npieces; ++issued) {
+          const int ch = issued / ncon, c = c_lo + issued % ncon, slot = issued % p.pslots;
+          const uint32_t bytes = static_cast<uint32_t>(min(32, p.m16 - ch * 32) / 4) * kTileN * 16;
+          mbar_arrive_expect_tx(&pbar[slot], bytes);
+          bulk_g2s(base + size_t(slot) * kPiece,
+                   part4 + (static_cast<size_t>(c) * nq + ch * 8) * kTileN, bytes, &pbar[slot]);
+        }
+      };
+      if (et == 0) issue(p.pslots);
+      const int n_base = sg.tile * kTileN;
+      // The last segment of the range has the ring to itself: its Y tile is
+      // built there whole and leaves by TMA store (no per-chunk barriers).
+      const bool tma_y = p.ytma && pos == r_end;
+      __nv_bfloat16* ytile = reinterpret_cast<__nv_bfloat16*>(base + p.ytile_off);
+      for (int c0 = 0, ch = 0; c0 < p.m16; c0 += 32, ++ch) {
+        const bool more = c0 + 32 < p.m16;
+        if (more) tmem_ld32_async(taddr + c0 + 32, rb);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ra[j]);
+        for (int ci = 0; ci < ncon; ++ci) {   // partials in CTA order
+          const int pidx = ch * ncon + ci, slot = pidx % p.pslots;
+          mbar_wait_bounded(&pbar[slot], (pidx / p.pslots) & 1, nullptr, p.status);
+          const float4* sp = reinterpret_cast<const float4*>(base + size_t(slot) * kPiece);
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (c0 + 4 * g < p.m16) {
+              const float4 u = sp[g * kTileN + row];
+              v[4 * g] += u.x;
+              v[4 * g + 1] += u.y;
+              v[4 * g + 2] += u.z;
+              v[4 * g + 3] += u.w;
+            }
+          // more partials than slots: refill after every full round of slots
+          if ((pidx + 1) % p.pslots == 0 && ci + 1 < ncon) {
+            epi_sync();
+            if (et == 0) issue(pidx + 1 + p.pslots);
+          }
+        }
+        if (tma_y) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < p.m16) ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(v[j]);
+          if (ncon) {   // every thread is done with this chunk's pieces: refill their slots
+            epi_sync();
+            if (et == 0) issue((ch + 1) * ncon + p.pslots);
+          }
+          if (more) {
+            tmem_ld_wait(rb);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ra[j] = rb[j];
+          }
+          continue;
+        }
+        // Y[c0 .. c0 + 31][n_base .. n_base + 127] through shared memory, 16
+        // tokens at a time, so that the global stores are 16-byte pieces of
+        // whole 256-byte rows
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ystage[j * kTileN + row] = __float2bfloat16_rn(v[16 * h + j]);
+          epi_sync();
+          // every thread is done with this chunk's pieces: refill their slots
+          if (h == 0 && et == 0 && ncon) issue((ch + 1) * ncon + p.pslots);
+#pragma unroll
+          for (int it = 0; it < 2; ++it) {
+            const int idx = it * 128 + et;
+            const int rr = idx >> 4, c8 = (idx & 15) * 8;
+            const int m = c0 + 16 * h + rr, n0 = n_base + c8;
+            if (m < p.M) {
+              const __nv_bfloat16* src = ystage + rr * kTileN + c8;
+              __nv_bfloat16* out = p.y + static_cast<size_t>(m) * p.N + n0;
+              if (p.yvec && n0 + 8 <= p.N) {
+                *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
+              } else {
+                for (int e = 0; e < 8; ++e)
+                  if (n0 + e < p.N) out[e] = src[e];
+              }
+            }
+          }
+          epi_sync();
+        }
+        if (more) {
+          tmem_ld_wait(rb);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ra[j] = rb[j];
+        }
+      }
+      if (tma_y) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        epi_sync();
+        if (et == 0) {
+          for (int rb0 = 0; rb0 < p.m16; rb0 += kYBoxRows)
+            tma_store_2d(&y_map, ytile + rb0 * kTileN, n_base, rb0);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty);
+      if (lane == 0) mbar_arrive(&tmem_empty[a]);
     }
   }
 
@@ -407,22 +761,85 @@ using namespace idlm;
 
 namespace {
 
+// CTAs of the stream-K grid at most: the SMs of the current device (one CTA
+// per SM), or 256 where no device can be queried.
+int max_grid() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    return 256;
+  }
+  return std::min(n, 256);
+}
+
+struct WsLayout {
+  size_t t64, b64, tpart, tcount, flag, part, total;
+};
+WsLayout ws_layout(int M, int K, int N) {
+  const int Ms = std::min(M, lora::kMaxTokens);
+  const size_t m16 = (Ms + 15) / 16 * 16;
+  const size_t ks = (K + lora::kTSlice - 1) / lora::kTSlice;
+  const size_t G = max_grid();
+  WsLayout l;
+  l.t64 = 0;
+  l.b64 = align_up(static_cast<size_t>(Ms) * lora::kPadW * 2, 256);
+  l.tpart = l.b64 + align_up(static_cast<size_t>(N) * lora::kPadW * 2, 256);
+  l.tcount = l.tpart + align_up(ks * m16 * lora::kPadW * sizeof(float), 256);
+  l.flag = l.tcount + align_up(m16 / 16 * sizeof(unsigned long long), 256);
+  l.part = l.flag + align_up(G * sizeof(unsigned long long), 256);
+  l.total = l.part + G * lora::kTileN * m16 * sizeof(float);
+  return l;
+}
+
 struct LoraPlan {
-  int m16, n1, n2, tiles, kb;
+  int m16, n1, n2, tiles, kb, S, stages, nacc, grid;
+  long long U;
   uint32_t stage_bytes;
   size_t smem;
 };
 
-LoraPlan plan_for(int M, int K, int N) {
+// Grid size of the stream-K split by a cost model in microseconds, fitted to
+// B300 timings of this kernel at 448 tokens: a K step of the 128 x 448 tile
+// takes about 0.63 us (the MMAs near the measured bf16 peak rate and the TMA
+// ingest of its 73 KB of operands); an epilogue that writes a Y tile about
+// 10 us, one that writes a 229 KB fp32 partial tile about 5 us, and a
+// finaliser about 10 us more per partial it adds.  All but a quarter of the
+// step and all of the epilogue scale with the tokens.  Every CTA's range
+// holds at least one unit, and the grid never exceeds the SMs, so that all
+// CTAs are resident at once (a finaliser waits for CTAs after it).
+LoraPlan plan_for(int M, int K, int N, int grid_cap) {
   LoraPlan pl;
   pl.m16 = (M + 15) / 16 * 16;
   pl.n1 = std::min(256, pl.m16);
   pl.n2 = pl.m16 - pl.n1;
   pl.tiles = (N + lora::kTileN - 1) / lora::kTileN;
   pl.kb = (K + lora::kBK - 1) / lora::kBK;
-  pl.stage_bytes = lora::kWBytes + static_cast<uint32_t>(pl.m16) * 128;
-  pl.stage_bytes = (pl.stage_bytes + 1023) / 1024 * 1024;
-  pl.smem = lora::smem_bytes(pl.stage_bytes);
+  pl.S = pl.kb + 1;
+  pl.U = static_cast<long long>(pl.tiles) * pl.S;
+  pl.stage_bytes = lora::kWBytes + static_cast<uint32_t>(pl.m16) * 128;   // 2 KB multiple
+  pl.nacc = pl.m16 <= static_cast<int>(lora::kAccCols) ? 2 : 1;
+  const double f = pl.m16 / 448.0;
+  const double step = 0.63 * (0.25 + 0.75 * f);
+  double best = 1e300;
+  pl.grid = 1;
+  const long long gmax = std::min<long long>(grid_cap, pl.U);
+  const char* force = std::getenv("IDLM_LORA_GRID");
+  if (force && std::atoll(force) > 0) {   // a fixed grid (the tests cover several)
+    pl.grid = static_cast<int>(std::min<long long>(gmax, std::atoll(force)));
+    return pl;
+  }
+  for (long long G = 1; G <= gmax; ++G) {
+    const long long per = (pl.U + G - 1) / G, minseg = pl.U / G;
+    const bool split = pl.U % G != 0 || (pl.U / G) % pl.S != 0;
+    const long long contrib = split ? (pl.S + minseg - 1) / minseg : 0;
+    const double ytiles = std::max(1.0, static_cast<double>(per) / pl.S);
+    const double t = per * step + (split ? (5.0 + 10.0 * contrib) * f : 0.0) + 10.0 * f * ytiles;
+    if (t < best * 0.98) {
+      best = t;
+      pl.grid = static_cast<int>(G);
+    }
+  }
   return pl;
 }
 
@@ -430,9 +847,7 @@ LoraPlan plan_for(int M, int K, int N) {
 
 extern "C" size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r) {
   if (M <= 0 || K <= 0 || N <= 0 || r <= 0) return 0;
-  const int Ms = std::min(M, lora::kMaxTokens);
-  return align_up(static_cast<size_t>(Ms) * lora::kPadW * 2, 256) +
-         align_up(static_cast<size_t>(N) * lora::kPadW * 2, 256);
+  return ws_layout(M, K, N).total;
 }
 
 extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void* lora_a,
@@ -447,7 +862,8 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
        reinterpret_cast<uintptr_t>(lora_a) | reinterpret_cast<uintptr_t>(lora_b)) & 15)
     return IDLM_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < idlm_gated_lora_workspace_size(M, K, N, r))
+  if (!workspace || workspace_bytes < idlm_gated_lora_workspace_size(M, K, N, r) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
     return IDLM_ERR_WORKSPACE;
   DeviceInfo dev;
   if (!current_device_info(&dev)) return IDLM_ERR_CUDA;
@@ -460,20 +876,36 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
       if (cudaFuncSetAttribute(lora::lora_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dev.max_smem_optin) != cudaSuccess)
         return IDLM_ERR_CUDA;
+      // the adapter kernel's CTAs run beside GEMM CTAs: keep the SM's
+      // shared-memory carveout at its maximum for both
+      if (cudaFuncSetAttribute(lora::lora_t_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return IDLM_ERR_CUDA;
       done[dev.device] = true;
     }
   }
-  __nv_bfloat16* t = static_cast<__nv_bfloat16*>(workspace);
-  __nv_bfloat16* b64 = reinterpret_cast<__nv_bfloat16*>(
-      static_cast<uint8_t*>(workspace) +
-      align_up(static_cast<size_t>(std::min(M, lora::kMaxTokens)) * lora::kPadW * 2, 256));
+  // launches get distinct epochs, so the flags never need clearing
+  static std::atomic<unsigned long long> epoch_counter{
+      0x9e3779b97f4a7c15ull ^
+      static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};
+  const WsLayout wl = ws_layout(M, K, N);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(wsb + wl.t64);
+  __nv_bfloat16* b64 = reinterpret_cast<__nv_bfloat16*>(wsb + wl.b64);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
-  // token rows in slices of at most 512 (the tensor-memory columns)
+  const int grid_cap = std::min(dev.sm_count, max_grid());
+  // token rows in slices of at most 448 (the tensor-memory columns and the ring)
   for (int m0 = 0; m0 < M; m0 += lora::kMaxTokens) {
     const int Ms = std::min(lora::kMaxTokens, M - m0);
-    const LoraPlan pl = plan_for(Ms, K, N);
-    if (pl.smem > static_cast<size_t>(dev.max_smem_optin)) return IDLM_ERR_UNSUPPORTED;
+    const LoraPlan pl = plan_for(Ms, K, N, grid_cap);
+    const int stages = std::min<int>(
+        lora::kMaxStages,
+        static_cast<int>((dev.max_smem_optin - 1024 - lora::kBarBytes - lora::kStageY) /
+                         pl.stage_bytes));
+    if (stages < 2) return IDLM_ERR_UNSUPPORTED;
+    // at least 120 KB, so that one CTA holds an SM (and its tensor memory)
+    const size_t smem = std::max<size_t>(lora::smem_bytes(stages, pl.stage_bytes), 120 * 1024);
     const __nv_bfloat16* xs = xb + static_cast<size_t>(m0) * K;
     CUtensorMap wm, xm1, xm2, bm, tm1, tm2;
     const uint64_t wdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
@@ -493,19 +925,35 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
         !encode_bf16_map(&tm2, t, 2, tdims, rstr, xbox2))
       return IDLM_ERR_CUDA;
 
-    const int tblocks = (Ms + lora::kTRows - 1) / lora::kTRows;
+    const unsigned long long epoch = ++epoch_counter;
+    lora::TParams tp;
+    tp.x = xs;
+    tp.a = static_cast<const __nv_bfloat16*>(lora_a);
+    tp.b = static_cast<const __nv_bfloat16*>(lora_b);
+    tp.gate = row_gate + m0;
+    tp.scale = lora_scale;
+    tp.M = Ms;
+    tp.K = K;
+    tp.N = N;
+    tp.r = r;
+    tp.kslices = (K + lora::kTSlice - 1) / lora::kTSlice;
+    tp.tpart = reinterpret_cast<float*>(wsb + wl.tpart);
+    tp.tcount = reinterpret_cast<unsigned long long*>(wsb + wl.tcount);
+    tp.epoch = epoch;
+    tp.t64 = t;
+    tp.b64 = b64;
+    const int tblocks = (Ms + lora::kTRows - 1) / lora::kTRows * tp.kslices;
     const int bblocks = (N + lora::kTThreads - 1) / lora::kTThreads;
-    lora::lora_t_kernel<<<tblocks + bblocks, lora::kTThreads, 0, stream>>>(
-        xs, static_cast<const __nv_bfloat16*>(lora_a), static_cast<const __nv_bfloat16*>(lora_b),
-        row_gate + m0, lora_scale, Ms, K, N, r, t, b64);
+    lora::lora_t_kernel<<<tblocks + bblocks, lora::kTThreads, 0, stream>>>(tp);
     if (cudaGetLastError() != cudaSuccess) return IDLM_ERR_CUDA;
 
     lora::Params p;
     p.y = yb + static_cast<size_t>(m0) * N;
-    p.row_gate = row_gate + m0;
+    p.part = reinterpret_cast<float*>(wsb + wl.part);
+    p.flag = reinterpret_cast<unsigned long long*>(wsb + wl.flag);
+    p.epoch = epoch;
     p.status = status;
     p.M = Ms;
-    p.K = K;
     p.N = N;
     p.r = r;
     p.m16 = pl.m16;
@@ -513,22 +961,42 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
     p.n2 = pl.n2;
     p.tiles = pl.tiles;
     p.kb = pl.kb;
+    p.S = pl.S;
+    p.U = pl.U;
+    p.stages = stages;
+    p.nacc = pl.nacc;
+    p.yvec = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0) ? 1 : 0;
+    const size_t ring = size_t(stages) * pl.stage_bytes;
+    const size_t ytile_bytes = size_t(pl.m16) * lora::kTileN * 2;
+    p.ytma = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0) ? 1 : 0;
+    p.ytile_off = static_cast<uint32_t>(p.ytma ? (ring - ytile_bytes) / 1024 * 1024 : ring);
+    p.pslots = std::min<int>(lora::kMaxPSlots, static_cast<int>(p.ytile_off / lora::kPiece));
+    if (p.pslots < 1) return IDLM_ERR_UNSUPPORTED;
+    CUtensorMap ym;
+    if (p.ytma) {
+      const uint64_t ydims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(Ms)};
+      const uint64_t ystr[1] = {static_cast<uint64_t>(N) * 2};
+      const uint32_t ybox[2] = {lora::kTileN, lora::kYBoxRows};
+      if (!encode_bf16_map(&ym, p.y, 2, ydims, ystr, ybox, 0)) return IDLM_ERR_CUDA;
+    } else {
+      ym = wm;   // unused
+    }
     p.stage_bytes = pl.stage_bytes;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(std::min(pl.tiles, dev.sm_count));
+    cfg.gridDim = dim3(pl.grid);
     cfg.blockDim = dim3(lora::kThreads);
-    cfg.dynamicSmemBytes = pl.smem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, wm, xm1, xm2, bm, tm1, tm2, p);
-    if (e != cudaSuccess) {
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, wm, xm1, xm2, bm, tm1, tm2, ym, p);
+    if (e != cudaSuccess) {   // without programmatic dependent launch
       (void)cudaGetLastError();
       cfg.numAttrs = 0;
-      e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, wm, xm1, xm2, bm, tm1, tm2, p);
+      e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, wm, xm1, xm2, bm, tm1, tm2, ym, p);
     }
     if (e != cudaSuccess) return IDLM_ERR_CUDA;
   }

@@ -56,6 +56,7 @@ def assert_close(got, ref):
 
 
 @pytest.mark.parametrize("M,K,N,r", [(21, 136, 200, 16), (3, 64, 128, 8), (3, 64, 256, 8),
+                                     (45, 320, 204, 8),
                                      (448, 512, 384, 16), (600, 256, 256, 16), (130, 320, 520, 64),
                                      (48, 4096, 128, 16)])
 def test_against_oracle_small(cuda_device, M, K, N, r):
@@ -104,3 +105,31 @@ def test_layer_projection_full_size_sampled(cuda_device, name):
     ref = np.array([isd.gated_lora(xs[m:m + 1], wf[n:n + 1], af, bf[n:n + 1], g[m:m + 1],
                                    inp["lora_scale"])[0, 0] for m, n in zip(ms, ns)])
     assert_close(y[ms, ns], ref)
+
+
+@pytest.mark.parametrize("M,K,N,r", [(448, 640, 520, 16), (130, 4096, 256, 64), (37, 192, 384, 8)])
+def test_every_grid_size_matches_the_oracle_and_repeats_bitwise(cuda_device, monkeypatch, M, K, N, r):
+    """The GEMM splits the (tile, K step) work evenly over its grid; a tile
+    cut by a range boundary is summed from fp32 partial tiles in CTA order.
+    Every grid size (1 CTA, ranges inside one tile, ranges across several
+    tiles) must match the oracle, and a repeated call with the same grid must
+    give the same bits."""
+    x, w, a, b, g = case(M, K, N, r, seed=11 + M)
+    ref = isd.gated_lora(f64(x), f64(w), f64(a), f64(b), g.numpy(), 1.0)
+    for grid in (1, 2, 3, 7, 19, 64, 148):
+        monkeypatch.setenv("IDLM_LORA_GRID", str(grid))
+        y1 = gpu_lora(x, w, a, b, g, 1.0)
+        assert_close(f64(y1), ref)
+        y2 = gpu_lora(x, w, a, b, g, 1.0)
+        assert torch.equal(y1, y2), f"grid {grid} not reproducible"
+
+
+def test_ungated_rows_bit_identical_under_a_split_k_sum(cuda_device, monkeypatch):
+    """With tiles whose K sum is split over several CTAs, rows with g = 0 must
+    still equal the base projection (lora_b = 0) bit for bit."""
+    monkeypatch.setenv("IDLM_LORA_GRID", "37")
+    x, w, a, b, g = case(448, 2048, 640, 16, seed=9, wstd=0.2)
+    y = gpu_lora(x, w, a, b, g, 1.0)
+    y0 = gpu_lora(x, w, a, torch.zeros_like(b), g, 1.0)
+    clean = (g == 0).cuda()
+    assert torch.equal(y[clean], y0[clean])
