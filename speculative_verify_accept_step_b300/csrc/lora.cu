@@ -567,8 +567,7 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
     // ---------------------------------------------------------- epilogue
     // Thread `row` (0..127) owns weight row tile * 128 + row: TMEM lane row.
     // Every decision that ends the loop is taken after epi_sync, from
-    // shared state, so the four warps always meet the same barriers.  The
-    // next 32 TMEM columns load while the current ones are written out.
+    // shared state, so the four warps always meet the same barriers.
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int et = tid - 64;   // 0..127
@@ -588,26 +587,19 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
       if (*epi_fail) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * kAccCols;
-      uint32_t ra[32], rb[32];
-      tmem_ld32_async(taddr, ra);
-      tmem_ld_wait(ra);
+      uint32_t ra[32];
       if (sg.k0 > 0) {
         // a partial tile: into this CTA's workspace slot, then the flag
         float4* dst = reinterpret_cast<float4*>(p.part) + static_cast<size_t>(blockIdx.x) * nq * kTileN;
         for (int c0 = 0; c0 < p.m16; c0 += 32) {
-          const bool more = c0 + 32 < p.m16;
-          if (more) tmem_ld32_async(taddr + c0 + 32, rb);
+          tmem_ld32_async(taddr + c0, ra);
+          tmem_ld_wait(ra);
 #pragma unroll
           for (int g = 0; g < 8; ++g)
             if (c0 + 4 * g < p.m16)
               __stcg(dst + static_cast<size_t>(c0 / 4 + g) * kTileN + row,
                      make_float4(__uint_as_float(ra[4 * g]), __uint_as_float(ra[4 * g + 1]),
                                  __uint_as_float(ra[4 * g + 2]), __uint_as_float(ra[4 * g + 3])));
-          if (more) {
-            tmem_ld_wait(rb);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ra[j] = rb[j];
-          }
         }
         tc_fence_before();
         __syncwarp();
@@ -657,8 +649,8 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
       const bool tma_y = p.ytma && pos == r_end;
       __nv_bfloat16* ytile = reinterpret_cast<__nv_bfloat16*>(base + p.ytile_off);
       for (int c0 = 0, ch = 0; c0 < p.m16; c0 += 32, ++ch) {
-        const bool more = c0 + 32 < p.m16;
-        if (more) tmem_ld32_async(taddr + c0 + 32, rb);
+        tmem_ld32_async(taddr + c0, ra);
+        tmem_ld_wait(ra);
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ra[j]);
@@ -689,11 +681,6 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
             epi_sync();
             if (et == 0) issue((ch + 1) * ncon + p.pslots);
           }
-          if (more) {
-            tmem_ld_wait(rb);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ra[j] = rb[j];
-          }
           continue;
         }
         // Y[c0 .. c0 + 31][n_base .. n_base + 127] through shared memory, 16
@@ -723,11 +710,6 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
             }
           }
           epi_sync();
-        }
-        if (more) {
-          tmem_ld_wait(rb);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ra[j] = rb[j];
         }
       }
       if (tma_y) {
