@@ -76,3 +76,34 @@ def test_bad_sizes_are_rejected_without_a_gpu(lib):
     rc = lib.idlm_kv_commit(dummy, dummy, dummy, 1, dummy, dummy, dummy, dummy, dummy, dummy,
                             1, 3, 1, 3, 16, 1, 0, None, dummy, None)
     assert rc == 2
+
+
+def test_gated_lora_host_checks_without_a_gpu(lib):
+    """idlm_gated_lora validates its arguments on the host, before any CUDA call."""
+    d = ctypes.c_void_p(256)      # 256-byte aligned, never dereferenced
+    odd = ctypes.c_void_p(264)    # 8-byte aligned only
+    ws = lib.idlm_gated_lora_workspace_size(448, 4096, 1024, 16)
+    assert ws > 0
+    # null pointers
+    assert lib.idlm_gated_lora(None, d, d, d, d, 1.0, 448, 4096, 1024, 16, d, d, ws, d, None) == 1
+    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 16, d, d, ws, None, None) == 1
+    # sizes: M = 0, K not a multiple of 8, r not a multiple of 8 or above 64
+    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 0, 4096, 1024, 16, d, d, ws, d, None) == 1
+    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4092, 1024, 16, d, d, ws, d, None) == 2
+    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 12, d, d, ws, d, None) == 2
+    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 72, d, d, ws, d, None) == 2
+    # operands must be 16-byte aligned (TMA)
+    assert lib.idlm_gated_lora(odd, d, d, d, d, 1.0, 448, 4096, 1024, 16, d, d, ws, d, None) == 1
+    # workspace: too small, or not 256-byte aligned
+    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 16, d, d, ws - 1, d, None) == 3
+    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 16, d, odd, ws, d, None) == 3
+
+
+def test_gated_lora_workspace_size(lib):
+    f = lib.idlm_gated_lora_workspace_size
+    assert f(0, 4096, 1024, 16) == 0 and f(448, 4096, 1024, 0) == 0
+    # grows with N (the padded B rows) and with K (the adapter's K-slice partials)
+    assert f(448, 4096, 2048, 16) > f(448, 4096, 1024, 16)
+    assert f(448, 8192, 1024, 16) > f(448, 4096, 1024, 16)
+    # token rows beyond one 448-row slice reuse the slice's workspace
+    assert f(4480, 4096, 1024, 16) == f(448, 4096, 1024, 16)
