@@ -629,7 +629,16 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
       // built there whole and leaves by TMA store (no per-chunk barriers).
       const bool tma_y = p.ytma && pos == r_end;
       __nv_bfloat16* ytile = reinterpret_cast<__nv_bfloat16*>(base + p.ytile_off);
-      for (int c0 = 0, ch = 0; c0 < p.m16; c0 += 32, ++ch) {
+      // The common case (a whole tile at the end of the range) gets a loop of
+      // its own: small enough to stay in the instruction cache.
+      for (int c0 = 0; tma_y && ncon == 0 && c0 < p.m16; c0 += 32) {
+        tmem_ld32_async(taddr + c0, ra);
+        tmem_ld_wait(ra);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < p.m16) ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(__uint_as_float(ra[j]));
+      }
+      for (int c0 = 0, ch = 0; !(tma_y && ncon == 0) && c0 < p.m16; c0 += 32, ++ch) {
         tmem_ld32_async(taddr + c0, ra);
         tmem_ld_wait(ra);
         float v[32];
