@@ -158,6 +158,9 @@ idlm_status idlm_isd_attention(
  * a persistent grid of at most one CTA per SM that splits the (tile, K
  * step) work evenly; where a tile's K sum is split, its partial sums are
  * added in a fixed order, so results are reproducible on a given device.
+ * A CTA that adds partial sums waits for the CTAs that produce them, so the
+ * grid relies on all its CTAs becoming resident: work from other streams
+ * that holds SMs for more than 2 s ends the call with TIMEOUT.
  * The environment variable IDLM_LORA_GRID, if set, fixes the grid size
  * (capped at the SMs).  Device errors: TIMEOUT.
  * ---------------------------------------------------------------------- */
