@@ -59,12 +59,15 @@ def peaks():
     return 6400.0, 1800.0, "fallback"
 
 
-def lora_leg(dev, reps=20):
+def lora_leg(dev, reps=20, fused=False):
     """The gated-LoRA projections of one decoder layer (workload lora_layer_m448:
     hidden 4096, FFN 12288, 448 token rows, rank 16, gate on at MASK rows),
     each through idlm_gated_lora, timed alone with CUDA events.  Returns
     per-projection and whole-layer TFLOP/s (algorithmic 2 M K N per
-    projection; the adapter's extra work is not counted)."""
+    projection; the adapter's extra work is not counted).  fused=True runs
+    the projections that share an input as one call each (q|k|v: N = 6144,
+    rank 48; gate|up: N = 24576, rank 32; B block diagonal), the same layer
+    arithmetic in four calls."""
     import speculative_verify_accept_step_b300 as L
     from speculative_verify_accept_step_b300 import workloads as wl
     w = wl.WORKLOADS["lora_layer_m448"]
@@ -73,9 +76,13 @@ def lora_leg(dev, reps=20):
     xf = torch.randn(w.T, w.ffn, generator=torch.Generator().manual_seed(3)).bfloat16().to(dev)
     gate = inp["row_gate"].to(dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
+    groups = ([("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")),
+               ("down", ("down",))] if fused else
+              [(n, (n,)) for n in ("q", "k", "v", "o", "gate", "up", "down")])
     out, tot_flop, tot_ms = {}, 0.0, 0.0
-    for name in ("q", "k", "v", "o", "gate", "up", "down"):
-        pj = {k: v.to(dev) for k, v in inp["proj"][name].items()}
+    for name, members in groups:
+        src = wl.fuse_projections(inp["proj"], members) if fused else inp["proj"][name]
+        pj = {k: v.to(dev) for k, v in src.items()}
         xi = xf if name == "down" else x
         M, K = xi.shape
         N, r = pj["w"].shape[0], pj["a"].shape[0]
@@ -95,7 +102,7 @@ def lora_leg(dev, reps=20):
         fl = 2.0 * M * K * N
         tot_flop += fl
         tot_ms += ms
-        out[name] = {"M": M, "K": K, "N": N, "us": ms * 1e3, "TFLOP/s": fl / ms / 1e9}
+        out[name] = {"M": M, "K": K, "N": N, "r": r, "us": ms * 1e3, "TFLOP/s": fl / ms / 1e9}
         del ws, y
     assert int(st.item()) == 0, f"device status {int(st.item())}"
     return {"workload": w.name, "projections": out, "layer_us": tot_ms * 1e3,
@@ -366,6 +373,12 @@ def run_ours(args):
         lora["peak"] = bf16
         lora["frac"] = lora["TFLOP/s"] / bf16
         lora["bound"] = "tensor"
+        try:   # the same layer with q|k|v and gate|up fused into one call each
+            lf = lora_leg(dev, fused=True)
+            lora["fused"] = {"layer_us": lf["layer_us"], "TFLOP/s": lf["TFLOP/s"],
+                             "frac": lf["TFLOP/s"] / bf16, "projections": lf["projections"]}
+        except Exception as e:   # reported, never fatal to the step's line
+            lora["fused"] = {"error": str(e)[:300]}
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.profile_run:
         cpu = cpu_baseline(w, st.host)

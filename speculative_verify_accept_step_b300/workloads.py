@@ -252,3 +252,23 @@ def lora_inputs(w, seed=0):
     pos = torch.arange(M) % (2 * w.N - 1)
     row_gate = (pos >= w.N).to(torch.uint8)
     return dict(x=x, proj=proj, row_gate=row_gate, lora_scale=1.0)
+
+
+def fuse_projections(proj, names):
+    """One projection equal to several that share their input (q|k|v, gate|up):
+    weights stacked along N, adapters stacked along the rank (A) with B block
+    diagonal, so row block i of the output is projection i's output (the
+    other blocks' adapter columns meet zeros in B).  Data layout only."""
+    ws = [proj[n]["w"] for n in names]
+    As = [proj[n]["a"] for n in names]
+    Bs = [proj[n]["b"] for n in names]
+    W = torch.cat(ws, 0)
+    A = torch.cat(As, 0)
+    B = torch.zeros(W.shape[0], sum(a.shape[0] for a in As), dtype=Bs[0].dtype)
+    n0 = r0 = 0
+    for b in Bs:
+        B[n0:n0 + b.shape[0], r0:r0 + b.shape[1]] = b
+        n0 += b.shape[0]
+        r0 += b.shape[1]
+    return dict(w=W, a=A, b=B)
+

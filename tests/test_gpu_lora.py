@@ -133,3 +133,30 @@ def test_ungated_rows_bit_identical_under_a_split_k_sum(cuda_device, monkeypatch
     y0 = gpu_lora(x, w, a, torch.zeros_like(b), g, 1.0)
     clean = (g == 0).cuda()
     assert torch.equal(y[clean], y0[clean])
+
+
+def test_fused_projections_match_the_separate_ones(cuda_device):
+    """q|k|v as one call (weights stacked along N, adapters stacked along the
+    rank with B block diagonal) gives each projection's output: compared with
+    the three separate calls within the tolerance, and with the oracle on
+    sampled outputs."""
+    w_ = wl.WORKLOADS["lora_layer_m448"]
+    inp = wl.lora_inputs(w_)
+    names = ("q", "k", "v")
+    f = wl.fuse_projections(inp["proj"], names)
+    yf = f64(gpu_lora(inp["x"], f["w"], f["a"], f["b"], inp["row_gate"], inp["lora_scale"]))
+    n0 = 0
+    for n in names:
+        pj = inp["proj"][n]
+        ys = f64(gpu_lora(inp["x"], pj["w"], pj["a"], pj["b"], inp["row_gate"], inp["lora_scale"]))
+        assert_close(yf[:, n0:n0 + ys.shape[1]], ys)
+        n0 += ys.shape[1]
+    assert n0 == yf.shape[1]
+    M, N = yf.shape
+    rng = np.random.default_rng(1)
+    ms, ns = rng.integers(0, M, 2048), rng.integers(0, N, 2048)
+    xs, wf, af, bf = f64(inp["x"]), f64(f["w"]), f64(f["a"]), f64(f["b"])
+    g = inp["row_gate"].numpy()
+    ref = np.array([isd.gated_lora(xs[m:m + 1], wf[n:n + 1], af, bf[n:n + 1], g[m:m + 1],
+                                   inp["lora_scale"])[0, 0] for m, n in zip(ms, ns)])
+    assert_close(yf[ms, ns], ref)
