@@ -149,12 +149,23 @@ def barrier(ws):
 
 
 def allreduce(x, ws, op):
+    """x reduced over the ranks (a host float); the tensor lives where the
+    process group's backend wants it (GPU for NCCL, host for gloo)."""
     if ws <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def aggregate(tokens_local, ms_local, ws):
+    """Whole-job throughput of replicas: every rank's tokens over the slowest
+    rank's time.  Returns (tokens, ms, tokens per second)."""
+    ms = allreduce(float(ms_local), ws, _max_op())
+    tokens = allreduce(float(tokens_local), ws, _sum_op())
+    return tokens, ms, tokens / (ms * 1e-3)
 
 
 # ------------------------------------------------------------- clock sampling
@@ -350,12 +361,11 @@ def run_ours(args):
     barrier(ws)
     clk = clocks.stop()
     ms_local = e0.elapsed_time(e1)
-    ms = allreduce(ms_local, ws, _max_op())
     assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
     n_out = torch.stack([o["n_out"] for o in outs]).sum().item()
     n_acc = torch.stack([o["n_accepted"] for o in outs]).sum().item()
     n_rej = torch.stack([(o["next_mode"] == 0).sum() for o in outs]).sum().item()
-    tokens = allreduce(float(n_out), ws, _sum_op())
+    tokens, ms, _ = aggregate(n_out, ms_local, ws)
     att_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     acc_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     com_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / K
@@ -482,9 +492,8 @@ def run_e2e(st, K, ws):
                 tokens += int(back["n_out"].sum())
         e1.record()
         torch.cuda.synchronize()
-    ms = allreduce(e0.elapsed_time(e1), ws, _max_op())
-    tokens = allreduce(float(tokens), ws, _sum_op())
-    return {"value": tokens / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    tokens, ms, rate = aggregate(tokens, e0.elapsed_time(e1), ws)
+    return {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K}
 
 
