@@ -52,3 +52,20 @@ def test_noise_table_meets_its_targets():
         y = torch.from_numpy(z + sigma * eps).bfloat16().double().numpy()
         overlap = np.minimum(p, softmax_t(y, 1.0)).sum(-1).mean()
         assert abs(overlap - target) < 0.03
+
+
+def test_fused_projections_are_exact():
+    """fuse_projections (q|k|v, gate|up as one call): stacked weights give the
+    separate base projections, and the block-diagonal adapter gives each block
+    exactly its own adapter term (float64 on a few rows)."""
+    w = wl.WORKLOADS["lora_layer_m448"]
+    inp = wl.lora_inputs(w)
+    x = inp["x"][:6].double()
+    for names in (("q", "k", "v"), ("gate", "up")):
+        f = wl.fuse_projections(inp["proj"], names)
+        assert f["a"].shape[0] == sum(inp["proj"][n]["a"].shape[0] for n in names)
+        fused = x @ f["w"].double().T + (x @ f["a"].double().T) @ f["b"].double().T
+        sep = torch.cat([x @ inp["proj"][n]["w"].double().T
+                         + (x @ inp["proj"][n]["a"].double().T) @ inp["proj"][n]["b"].double().T
+                         for n in names], 1)
+        assert torch.equal(fused, sep) or float((fused - sep).abs().max()) < 1e-12
