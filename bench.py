@@ -498,44 +498,97 @@ def run_e2e(st, K, ws):
 
 
 # ------------------------------------------------------------- CPU baseline
+#
+# The oracle (numpy float64) as it stands, timed on the host's cores.  The
+# step's host tensors are placed once in shared memory; each worker process
+# (spawned, one BLAS thread each) attaches to it and runs the oracle's full
+# step (attention, accept, commit) for whole requests.
 
-def _oracle_step(host, w, requests, step):
-    """The oracle's full step for a subset of requests; returns tokens emitted."""
+def _bf16_to_f64(a):
+    """bf16 bits (int16 array) or float32 array -> float64."""
+    import numpy as np
+    if a.dtype == np.int16:
+        return (a.astype(np.int32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+class SharedBatch:
+    """The host tensors of one step in one shared-memory block (numpy views)."""
+    KEYS = ("q", "k_new", "v_new", "k_cache", "v_cache", "page_table", "seq_lens", "qo_indptr",
+            "logits0", "logits1", "qo0", "qo1")
+
+    def __init__(self, host):
+        import numpy as np
+        from multiprocessing import shared_memory
+        a, b = host["a"], host["b"]
+        src = {k: (a if k in a else b)[k] for k in self.KEYS}
+        arrs = {k: (t.view(torch.int16) if t.dtype == torch.bfloat16 else t).numpy()
+                for k, t in src.items()}
+        self.meta, off = {}, 0
+        for k, x in arrs.items():
+            self.meta[k] = (off, x.shape, x.dtype.str)
+            off += (x.nbytes + 63) // 64 * 64
+        self.shm = shared_memory.SharedMemory(create=True, size=max(off, 64))
+        for k, x in arrs.items():
+            o, shp, dt = self.meta[k]
+            np.ndarray(shp, dtype=dt, buffer=self.shm.buf, offset=o)[...] = x
+        self.name = self.shm.name
+
+    def close(self):
+        self.shm.close()
+        self.shm.unlink()
+
+
+_WORKER = {}
+
+
+def _worker_init(name, meta, wdict):
+    import numpy as np
+    from multiprocessing import shared_memory
+    sys.path.insert(0, ROOT)
+    shm = shared_memory.SharedMemory(name=name)
+    _WORKER["shm"] = shm
+    _WORKER["arr"] = {k: np.ndarray(shp, dtype=dt, buffer=shm.buf, offset=o)
+                      for k, (o, shp, dt) in meta.items()}
+    _WORKER["w"] = wdict
+
+
+def _oracle_request(arr, w, c, step):
+    """The oracle's full step for request c; returns the tokens it emits."""
     import numpy as np
     from oracle import isd
-    a, b = host["a"], host["b"]
-    f64 = lambda t: t.float().numpy().astype(np.float64)
-    qo = a["qo_indptr"].numpy()
-    M = w.N - 1
-    kc, vc = a["k_cache"], a["v_cache"]
-    emitted = 0
-    for c in requests:
-        t0, t1 = qo[c], qo[c + 1]
-        pages = a["page_table"][c]
-        used = pages[pages >= 0].long()
-        # gather only this request's pages for the oracle
-        remap = torch.full((int(a["num_pages"]),), -1, dtype=torch.long)
-        remap[used] = torch.arange(used.numel())
-        table = np.where(pages.numpy() >= 0, remap[pages.clamp(min=0).long()].numpy(), -1)
-        isd.isd_attention(f64(a["q"][t0:t1]), f64(a["k_new"][t0:t1]), f64(a["v_new"][t0:t1]),
-                          f64(kc[used]), f64(vc[used]), table[None], a["seq_lens"][c:c + 1].numpy(),
-                          np.array([0, t1 - t0]), w.page_size, a["sm_scale"])
-        r0 = b["qo0"][c].item()
-        r1 = b["qo1"][c].item()
-        l0 = f64(b["logits0"][r0:r0 + w.N])
-        l1 = f64(b["logits1"][r1:r1 + 2 * w.N - 1])
-        o0 = isd.isd_accept(l0, np.array([0, w.N]), np.array([isd.FRESH]), np.full((1, M), -1),
-                            l0, np.zeros(1, dtype=np.int64), w.N, w.temperature,
-                            isd.PROPOSE_ARGMAX, 0, 0, request_ids=np.array([c]))
-        o1 = isd.isd_accept(l1, np.array([0, 2 * w.N - 1]), o0["next_mode"], o0["next_drafts"],
-                            l0, o0["next_mask_row0"], w.N, w.temperature, isd.PROPOSE_ARGMAX, 0,
-                            step, request_ids=np.array([c]))
-        n = int(o1["n_commit"][0])
-        isd.kv_commit(f64(kc[used]), f64(vc[used]), table[None], a["seq_lens"][c:c + 1].numpy(),
-                      f64(a["k_new"][t0:t1]), f64(a["v_new"][t0:t1]), np.array([0, t1 - t0]),
-                      np.array([n]), w.page_size)
-        emitted += int(o1["n_out"][0])
-    return emitted
+    N, P = w["N"], w["page_size"]
+    M = N - 1
+    qo = arr["qo_indptr"]
+    t0, t1 = int(qo[c]), int(qo[c + 1])
+    pages = arr["page_table"][c]
+    used = pages[pages >= 0].astype(np.int64)
+    table = np.full(pages.shape, -1, dtype=np.int64)
+    table[:used.size] = np.arange(used.size)      # the request's pages, in table order
+    kc = _bf16_to_f64(arr["k_cache"][used])
+    vc = _bf16_to_f64(arr["v_cache"][used])
+    q = _bf16_to_f64(arr["q"][t0:t1])
+    kn = _bf16_to_f64(arr["k_new"][t0:t1])
+    vn = _bf16_to_f64(arr["v_new"][t0:t1])
+    sl = arr["seq_lens"][c:c + 1].astype(np.int64)
+    sub_qo = np.array([0, t1 - t0])
+    isd.isd_attention(q, kn, vn, kc, vc, table[None], sl, sub_qo, P, w["sm_scale"])
+    r0, r1 = int(arr["qo0"][c]), int(arr["qo1"][c])
+    l0 = _bf16_to_f64(arr["logits0"][r0:r0 + N])
+    l1 = _bf16_to_f64(arr["logits1"][r1:r1 + 2 * N - 1])
+    o0 = isd.isd_accept(l0, np.array([0, N]), np.array([isd.FRESH]), np.full((1, M), -1),
+                        l0, np.zeros(1, dtype=np.int64), N, w["temperature"],
+                        isd.PROPOSE_ARGMAX, 0, 0, request_ids=np.array([c]))
+    o1 = isd.isd_accept(l1, np.array([0, 2 * N - 1]), o0["next_mode"], o0["next_drafts"],
+                        l0, o0["next_mask_row0"], N, w["temperature"], isd.PROPOSE_ARGMAX, 0,
+                        step, request_ids=np.array([c]))
+    isd.kv_commit(kc, vc, table[None], sl, kn, vn, sub_qo, np.array([int(o1["n_commit"][0])]), P)
+    return int(o1["n_out"][0])
+
+
+def _worker_task(task):
+    c, step = task
+    return _oracle_request(_WORKER["arr"], _WORKER["w"], c, step)
 
 
 def _blas_threads():
@@ -546,17 +599,95 @@ def _blas_threads():
         return 1
 
 
-def cpu_baseline(w, host, budget_s=15.0):
-    """The oracle as it stands, on a bounded sample of the same batch."""
-    t0 = time.time()
-    tokens, req, step = 0, 0, 1
-    while time.time() - t0 < budget_s and req < w.C:
-        tokens += _oracle_step(host, w, [req], step)
-        req += 1
-    dt = time.time() - t0
-    return {"value": tokens / dt, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"full step (attention, accept, commit) for {req} of {w.C} requests, "
-                      f"{dt:.1f} s, numpy float64"}
+def host_cpu():
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except AttributeError:
+        usable = os.cpu_count() or 1
+    return {"nproc": os.cpu_count(), "usable_cores": usable, "model": model}
+
+
+def _wdict(w, host):
+    return {"N": w.N, "page_size": w.page_size, "sm_scale": host["a"]["sm_scale"],
+            "temperature": w.temperature}
+
+
+def cpu_baseline(w, host, budget_s=12.0, one_core_s=8.0):
+    """The oracle as it stands, on a bounded sample of the same batch: on every
+    usable host core (a spawned process pool, one BLAS thread per process,
+    whole requests as tasks) and on one core.  `value` is the all-cores
+    figure; `cores` the processes that ran."""
+    import multiprocessing as mp
+    cpu = host_cpu()
+    sb = SharedBatch(host)
+    wd = _wdict(w, host)
+    try:
+        # one core: this process, BLAS held to one thread
+        import contextlib
+        try:
+            from threadpoolctl import threadpool_limits
+            one = threadpool_limits(limits=1)
+        except Exception:
+            one = contextlib.nullcontext()
+        arr = _attach(sb)
+        with one:
+            t0 = time.time()
+            tok1 = req1 = 0
+            while time.time() - t0 < one_core_s and req1 < w.C:
+                tok1 += _oracle_request(arr, wd, req1, 1)
+                req1 += 1
+            dt1 = time.time() - t0
+        del arr
+        # every usable core: spawned workers (safe after CUDA is initialised)
+        P = cpu["usable_cores"]
+        env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+        saved = {k: os.environ.get(k) for k in env_keys}
+        for k in env_keys:
+            os.environ[k] = "1"
+        try:
+            ctx = mp.get_context("spawn")
+            with ctx.Pool(P, initializer=_worker_init, initargs=(sb.name, sb.meta, wd)) as pool:
+                pool.map(_worker_task, [(c % w.C, 1) for c in range(P)])   # warm-up, untimed
+                t0 = time.time()
+                tokP = doneP = 0
+                tasks = ((i % w.C, 2 + i // w.C) for i in range(10 ** 9))
+                pending = [pool.apply_async(_worker_task, (next(tasks),)) for _ in range(2 * P)]
+                while pending:
+                    r = pending.pop(0)
+                    tokP += r.get()
+                    doneP += 1
+                    if time.time() - t0 < budget_s:
+                        pending.append(pool.apply_async(_worker_task, (next(tasks),)))
+                dtP = time.time() - t0
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+    finally:
+        sb.close()
+    return {"value": tokP / dtP, "unit": "tokens/s", "cores": P, "kind": "oracle",
+            "nproc": cpu["nproc"], "cpu_model": cpu["model"],
+            "sample": f"all cores: {doneP} whole-request steps (attention, accept, commit) of the "
+                      f"{w.C}-request batch in {dtP:.1f} s on {P} processes (one BLAS thread "
+                      f"each); one core: {req1} requests in {dt1:.1f} s; numpy float64",
+            "one_core": {"value": tok1 / dt1, "unit": "tokens/s", "cores": 1}}
+
+
+def _attach(sb):
+    import numpy as np
+    return {k: np.ndarray(shp, dtype=dt, buffer=sb.shm.buf, offset=o)
+            for k, (o, shp, dt) in sb.meta.items()}
 
 
 def run_reference(args):
@@ -566,28 +697,36 @@ def run_reference(args):
     from speculative_verify_accept_step_b300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
     host = dict(a=wl.attention_inputs(w), b=wl.accept_inputs(w))
-    per_step = 1     # requests per reference step: a bounded sample of the batch
-    for i in range(args.warmup):
-        _oracle_step(host, w, [i % w.C], i + 1)
-    t0 = time.time()
-    tokens = 0
-    done = 0
-    for k in range(args.steps):
-        tokens += _oracle_step(host, w, [(k * per_step) % w.C], k + 1)
-        done += 1
-        if time.time() - t0 > 150.0:   # keep the whole run within a few minutes
-            break
-    dt = time.time() - t0
+    sb = SharedBatch(host)
+    arr, wd = _attach(sb), _wdict(w, host)
+    try:
+        for i in range(args.warmup):
+            _oracle_request(arr, wd, i % w.C, i + 1)
+        t0 = time.time()
+        tokens = done = 0
+        for k in range(args.steps):
+            # a bounded sample of the batch per step: one request
+            tokens += _oracle_request(arr, wd, k % w.C, k + 1)
+            done += 1
+            if time.time() - t0 > 150.0:   # keep the whole run within a few minutes
+                break
+        dt = time.time() - t0
+    finally:
+        del arr
+        sb.close()
     v = tokens / dt
+    cpu = host_cpu()
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": done, "steps_requested": args.steps,
-        "warmup": args.warmup, "ms_per_step": dt / done * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes of the workload)",
+        "warmup": args.warmup, "ms_per_step": dt / done * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes of the workload)",
         "config": {"workload": w.name, "C": w.C, "N": w.N, "V": w.V},
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _blas_threads(),
+                         "kind": "oracle", "nproc": cpu["nproc"], "cpu_model": cpu["model"],
                          "sample": f"one request of {w.C} per step (full step: attention, "
-                                   "accept, commit), numpy float64"},
+                                   "accept, commit), numpy float64, this process"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 

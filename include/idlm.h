@@ -28,8 +28,7 @@
  *     state between calls.
  *   - Tensors are dense row-major ("C order") with the shapes given.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL means the
- *     legacy default stream).  They launch kernels and, where stated, one
- *     cudaMemsetAsync of the workspace; nothing else.
+ *     legacy default stream).  They launch kernels and nothing else.
  *   - The return value reports what the host can check before launching
  *     (argument ranges, workspace size, unsupported shapes) and launch
  *     errors.  On a non-OK return nothing was launched, except for
@@ -162,7 +161,12 @@ idlm_status idlm_isd_attention(
  * grid relies on all its CTAs becoming resident: work from other streams
  * that holds SMs for more than 2 s ends the call with TIMEOUT.
  * The environment variable IDLM_LORA_GRID, if set, fixes the grid size
- * (capped at the SMs).  Device errors: TIMEOUT.
+ * (capped at the SMs).  Device errors: TIMEOUT.  Failure-detection test
+ * switch: with IDLM_TEST_STALE_FLAGS=1 in the environment, a CTA that adds
+ * partial sums waits (for 20 ms) for a flag value that is never written, so
+ * any call whose grid splits a tile's K sum ends with TIMEOUT in `status`
+ * and leaves that tile's Y unwritten; the call still returns normally and
+ * the CUDA context stays usable.
  * ---------------------------------------------------------------------- */
 size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r);
 
@@ -251,7 +255,10 @@ idlm_status idlm_isd_accept(
  * process exits.  The call allocates nothing and frees nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is cached per CUDA context
+ *     (keyed on the context's unique id): after cudaDeviceReset, or under
+ *     another context on the same device, the next call looks it up again,
+ *     so make that call, too, outside a stream capture.
  *   - Returns IDLM_ERR_WORKSPACE, launching nothing, when the call needs more
  *     than 4 MiB, i.e. when idlm_isd_accept_workspace_size(C, T, N, V)
  *     exceeds 4194304 bytes.

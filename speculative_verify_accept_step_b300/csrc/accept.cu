@@ -1028,13 +1028,15 @@ size_t workspace_bytes(int C, int T, int V, int dtype, Params* p, void* base) {
 
 template <typename T>
 idlm_status launch(const Params& p, int dev, int sm_count, cudaStream_t stream) {
-  // shared-memory opt-in, once per device
+  // shared-memory opt-in, once per device and context (a reset context
+  // forgets function attributes)
   static std::mutex mu;
-  static bool done[64] = {};
+  static unsigned long long done[64] = {};
+  const unsigned long long ctx = current_context_id();
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= 64) return IDLM_ERR_CUDA;
-    if (!done[dev]) {
+    if (done[dev] != ctx || ctx == 0) {
       // all three kernels ask for the largest shared-memory carveout, so that
       // CTAs of kernels 2 and 3 may share an SM with a kernel-1 CTA
       if (cudaFuncSetAttribute(vocab_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1047,7 +1049,7 @@ idlm_status launch(const Params& p, int dev, int sm_count, cudaStream_t stream) 
           cudaFuncSetAttribute(work_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return IDLM_ERR_CUDA;
-      done[dev] = true;
+      done[dev] = ctx;
     }
   }
   const long long W = static_cast<long long>(p.T) * p.CH;
@@ -1174,21 +1176,28 @@ static __device__ __align__(256) uint8_t g_accept_scratch[kStaticScratchBytes];
 namespace {
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[64] = {};
+unsigned long long g_scratch_ctx[64] = {};
 }  // namespace
 
-// Device address of g_accept_scratch on the current device, looked up once
-// per device.  In host code the array's name is only a host-side handle; the
-// kernels need the address cudaGetSymbolAddress returns.
+// Device address of g_accept_scratch in the current context, looked up once
+// per context.  In host code the array's name is only a host-side handle; the
+// kernels need the address cudaGetSymbolAddress returns.  The cache is keyed
+// on the context's unique id, so after cudaDeviceReset (or under another
+// context on the same device) the address is looked up again instead of
+// reusing one from a context that no longer exists.  Where the driver gives
+// no context id, every call looks the address up.
 void* static_scratch() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
-  }
-  return g_scratch_ptr[dev];
+  if (g_scratch_ptr[dev] && ctx != 0 && g_scratch_ctx[dev] == ctx) return g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess) return nullptr;
+  if (ctx == 0) ctx = current_context_id();   // the look-up made the context current
+  g_scratch_ptr[dev] = p;
+  g_scratch_ctx[dev] = ctx;
+  return p;
 }
 
 }  // namespace acc

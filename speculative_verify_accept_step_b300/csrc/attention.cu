@@ -11,8 +11,8 @@
 // kv head) pair.  Its G * R query rows (R rows per request, G query heads per
 // kv head; 28 at N = 4) are packed into MT m-tiles of 16 rows, so every KV
 // byte is read from HBM once per unit and reused by all of them.  Work is the
-// list of 16-key blocks of all units (every cached page, plus one block of the
-// step's own new rows per unit); a persistent grid splits that list evenly
+// list of 16-key blocks of all units (every cached page, then ceil(R / 16)
+// blocks of the step's own new rows); a persistent grid splits that list evenly
 // (balanced split-KV), so long and short contexts load the SMs equally.
 // Units cut by a CTA boundary write partial (max, sum, O) triples to the
 // workspace and the last CTA to finish a unit (atomic arrival count, no
@@ -28,6 +28,8 @@
 // The general path (fp32, or any other D / page size) is a plain kernel with
 // one warp per (row, head) walking the keys in order.
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 
 #include "common.cuh"
 #include "host_util.h"
@@ -51,7 +53,8 @@ struct Params {
   const int32_t* qo_indptr;
   float* ws_o;       // [B][2][MT*16][D]
   float* ws_ml;      // [B][2][MT*16][2]
-  int32_t* ws_cnt;   // [C*Hkv]
+  unsigned long long* ws_cnt;   // [C*Hkv]: launch epoch << 32 | parts merged
+  unsigned long long epoch;     // distinct for every launch (low 32 bits used)
   int32_t* status;
   int max_pages, C, T, Hq, Hkv, G, num_pages, max_rows;
   float scale_log2;  // sm_scale * log2(e)
@@ -75,12 +78,21 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
 }
 
 // Position in the global block list -> (request, kv head, block-in-unit).
+// A unit's blocks are its nbc cached pages, then its blocks of new rows.
 struct Cursor {
-  int c, g, k, nb;
+  int c, g, k, nb, nbc;
   long long unit_start;
 };
 
-__device__ __forceinline__ Cursor locate(const int* pref, int C, int Hkv, long long j) {
+// Cached 16-key blocks of request c: ceil(L_c / 16), L_c clamped to the
+// request's page-table row.
+__device__ __forceinline__ int cached_blocks(const Params& p, int c) {
+  const int L = min(max(p.seq_lens[c], 0), p.max_pages * PS);
+  return (L + PS - 1) / PS;
+}
+
+__device__ __forceinline__ Cursor locate(const Params& p, const int* pref, int C, int Hkv,
+                                         long long j) {
   // largest c with Hkv * pref[c] <= j
   int lo = 0, hi = C - 1;
   while (lo < hi) {
@@ -94,17 +106,21 @@ __device__ __forceinline__ Cursor locate(const int* pref, int C, int Hkv, long l
   cur.g = static_cast<int>(rel / cur.nb);
   cur.k = static_cast<int>(rel % cur.nb);
   cur.unit_start = static_cast<long long>(Hkv) * pref[lo] + static_cast<long long>(cur.g) * cur.nb;
+  cur.nbc = cached_blocks(p, lo);
   return cur;
 }
 
-__device__ __forceinline__ void advance(Cursor& cur, const int* pref, int Hkv) {
+// Next block; past the last request's last block the cursor is not read.
+__device__ __forceinline__ void advance(Cursor& cur, const Params& p, const int* pref, int C,
+                                        int Hkv) {
   if (++cur.k < cur.nb) return;
   cur.k = 0;
   cur.unit_start += cur.nb;
   if (++cur.g < Hkv) return;
   cur.g = 0;
-  ++cur.c;
+  if (++cur.c >= C) return;
   cur.nb = pref[cur.c + 1] - pref[cur.c];
+  cur.nbc = cached_blocks(p, cur.c);
 }
 
 __device__ __forceinline__ long long range_lo(long long W, int B, int b) {
@@ -138,7 +154,8 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
   const int lane = tid & 31;
   const int C = p.C;
 
-  // ---- blocks per request: ceil(L / 16) cached pages + 1 block of new rows
+  // ---- blocks per request: ceil(L / 16) cached pages + ceil(R / 16) blocks
+  // of new rows (at least one, so that every unit has a block)
   if (tid == 0) {
     flags[0] = 0;
     flags[1] = 0;
@@ -160,7 +177,8 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
         set_status(p.status, IDLM_DEV_BAD_LAYOUT);
       if (L > p.max_pages * PS) set_status(p.status, IDLM_DEV_SLOT_OVERFLOW);
       L = min(max(L, 0), p.max_pages * PS);
-      pref[c + 1] = (L + PS - 1) / PS + 1;   // temporarily the count
+      const int R = min(max(rows, 0), p.max_rows);
+      pref[c + 1] = (L + PS - 1) / PS + max(1, (R + PS - 1) / PS);   // temporarily the count
       sum += pref[c + 1];
     }
     __syncthreads();
@@ -199,7 +217,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
       prefetch_tensormap(&vc_map);
       prefetch_tensormap(&kn_map);
       prefetch_tensormap(&vn_map);
-      Cursor cur = locate(pref, C, p.Hkv, lo);
+      Cursor cur = locate(p, pref, C, p.Hkv, lo);
       int issued = 0;
       for (long long j = lo; j < hi; ++j) {
         const int s = issued % STAGES;
@@ -207,8 +225,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
         if (!mbar_wait_bounded(&empty[s], ph ^ 1, flags, p.status)) break;
         uint8_t* dst = stages + s * STAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-        const int nbc = cur.nb - 1;
-        if (cur.k < nbc) {
+        if (cur.k < cur.nbc) {
           const int page = p.page_table[static_cast<size_t>(cur.c) * p.max_pages + cur.k];
           int y;
           if (page < 0 || page >= p.num_pages) {
@@ -222,14 +239,15 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
           tma_load_2d(dst + 2 * BOX_BYTES, &vc_map, &full[s], 0, y);
           tma_load_2d(dst + 3 * BOX_BYTES, &vc_map, &full[s], 64, y);
         } else {
-          const int t0 = p.qo_indptr[cur.c];
+          // new rows 16 b .. 16 b + 15 of the request (rows past T read zeros)
+          const int t0 = p.qo_indptr[cur.c] + PS * (cur.k - cur.nbc);
           tma_load_3d(dst, &kn_map, &full[s], 0, cur.g, t0);
           tma_load_3d(dst + BOX_BYTES, &kn_map, &full[s], 64, cur.g, t0);
           tma_load_3d(dst + 2 * BOX_BYTES, &vn_map, &full[s], 0, cur.g, t0);
           tma_load_3d(dst + 3 * BOX_BYTES, &vn_map, &full[s], 64, cur.g, t0);
         }
         ++issued;
-        advance(cur, pref, p.Hkv);
+        advance(cur, p, pref, C, p.Hkv);
       }
       // every issued copy must land before the CTA may exit
       for (int i = max(0, issued - STAGES); i < issued; ++i)
@@ -253,7 +271,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
   const int vkey = lane & 15;
   const int vch_off = lane >> 4;
 
-  Cursor cur = locate(pref, C, p.Hkv, lo < hi ? lo : 0);
+  Cursor cur = locate(p, pref, C, p.Hkv, lo < hi ? lo : 0);
   long long j = lo;
   int i = 0;
   while (j < hi) {
@@ -266,7 +284,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
     const int t0 = min(max(p.qo_indptr[c], 0), p.T);
     const int R = min(min(max(p.qo_indptr[c + 1] - t0, 0), p.max_rows), p.T - t0);
     const bool va = r_a < R, vb = r_b < R;
-    const int nbc = cur.nb - 1;
+    const int nbc = cur.nbc, nb = cur.nb;
 
     // Q fragments of this m-tile (rows past R are zero)
     uint32_t qa[8][4];
@@ -290,7 +308,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
 
-    for (; j < seg_end; ++j, ++i, advance(cur, pref, p.Hkv)) {
+    for (; j < seg_end; ++j, ++i, advance(cur, p, pref, C, p.Hkv)) {
       if ((i & 1) != par) continue;
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
@@ -313,8 +331,9 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
           mma_bf16_16816(sc[1], qa[ks], b2, b3);
         }
         // mask keys past the request's context (cached pages) or past the
-        // row's own position (the step's new rows); a full cached page needs
-        // no mask.  Column key = 8n + qc + e.
+        // row's own position (the step's new rows, block b = k - nbc holds
+        // rows 16 b ..); a full cached page needs no mask.  Column key =
+        // 8n + qc + e.
         const int k = cur.k;
         const bool full_page = k < nbc && (k + 1) * PS <= L;
         if (!full_page) {
@@ -327,8 +346,9 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
               if (k < nbc) {
                 ka = kb = (k * PS + key) < L;
               } else {
-                ka = key <= r_a;
-                kb = key <= r_b;
+                const int nr = PS * (k - nbc) + key;
+                ka = nr <= r_a;
+                kb = nr <= r_b;
               }
               if (!ka) sc[n][e] = kNegInf;
               if (!kb) sc[n][2 + e] = kNegInf;
@@ -465,17 +485,27 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
         __threadfence();
         named_bar(1 + MT, 32 * MT);
         const int u = c * p.Hkv + g;
-        const long long ustart = unit_end - (nbc + 1);
+        const long long ustart = unit_end - nb;
         const int bf = owner_of(W, B, ustart);
         const int bl = owner_of(W, B, unit_end - 1);
         if (mt == 0 && lane == 0) {
-          // CTAs with an empty range (more CTAs than blocks) hold no part
+          // CTAs with an empty range (more CTAs than blocks) hold no part.
+          // The counter carries this launch's epoch in its high half, so a
+          // count left by an earlier launch reads as zero (no clearing).
           int parts = 0;
           for (int b = bf; b <= bl; ++b) parts += range_lo(W, B, b) < range_lo(W, B, b + 1);
-          const int old = atomicAdd(&p.ws_cnt[u], 1);
-          const int last = (old == parts - 1);
-          if (last) p.ws_cnt[u] = 0;
-          flags[1] = last;
+          const unsigned long long tag = (p.epoch & 0xffffffffull) << 32;
+          unsigned long long* cnt = p.ws_cnt + u;
+          unsigned long long seen, old = *reinterpret_cast<volatile unsigned long long*>(cnt);
+          do {
+            seen = old;
+            const unsigned long long nv =
+                ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
+            old = atomicCAS(cnt, seen, nv);
+          } while (old != seen);
+          const unsigned long long now =
+              ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
+          flags[1] = (now & 0xffffffffull) == static_cast<unsigned long long>(parts);
         }
         named_bar(1 + MT, 32 * MT);
         const bool last = flags[1] != 0;
@@ -617,7 +647,7 @@ size_t workspace_for(int C, int Hkv, int B) {
   Carver cv(nullptr);
   cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * D);
   cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * 2);
-  cv.take<int32_t>(static_cast<size_t>(C) * Hkv);
+  cv.take<unsigned long long>(static_cast<size_t>(C) * Hkv);
   return cv.used;
 }
 
@@ -657,7 +687,12 @@ idlm_status launch_fast(const DeviceInfo& dev, const void* q, const void* k_new,
   Params p;
   p.ws_o = cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * D);
   p.ws_ml = cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * 2);
-  p.ws_cnt = cv.take<int32_t>(static_cast<size_t>(C) * Hkv);
+  p.ws_cnt = cv.take<unsigned long long>(static_cast<size_t>(C) * Hkv);
+  // launches get distinct epochs, so the merge counters never need clearing
+  static std::atomic<unsigned long long> epoch_counter{
+      0x2545f4914f6cdd1dull ^
+      static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};
+  p.epoch = ++epoch_counter;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.page_table = page_table;
@@ -689,8 +724,6 @@ idlm_status launch_fast(const DeviceInfo& dev, const void* q, const void* k_new,
       !encode_bf16_map(&vn, const_cast<void*>(v_new), 3, ndims, nstr, nbox))
     return IDLM_ERR_CUDA;
 
-  cudaError_t e = cudaMemsetAsync(p.ws_cnt, 0, static_cast<size_t>(C) * Hkv * sizeof(int32_t), stream);
-  if (e != cudaSuccess) return IDLM_ERR_CUDA;
   paged_attn_kernel<MT><<<B, Layout<MT>::kThreads, Layout<MT>::bytes(C), stream>>>(kc, vc, kn, vn, p);
   return cuda_status(cudaGetLastError());
 }

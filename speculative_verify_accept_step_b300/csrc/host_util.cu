@@ -8,6 +8,7 @@ namespace idlm {
 namespace {
 constexpr int kMaxDevices = 64;
 DeviceInfo g_info[kMaxDevices];
+unsigned long long g_ctx[kMaxDevices] = {};
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 }  // namespace
@@ -15,8 +16,9 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool current_device_info(DeviceInfo* out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_info[dev].device != dev) {
+  if (g_info[dev].device != dev || g_ctx[dev] != ctx || ctx == 0) {
     DeviceInfo d;
     d.device = dev;
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -25,6 +27,7 @@ bool current_device_info(DeviceInfo* out) {
         cudaSuccess)
       return false;
     g_info[dev] = d;
+    g_ctx[dev] = ctx;
   }
   *out = g_info[dev];
   return true;
@@ -41,6 +44,36 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   return g_encode;
+}
+
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!get_current || !get_id) {
+      void* f1 = nullptr;
+      void* f2 = nullptr;
+      cudaDriverEntryPointQueryResult q1, q2;
+      if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) !=
+              cudaSuccess ||
+          q1 != cudaDriverEntryPointSuccess ||
+          cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+              cudaSuccess ||
+          q2 != cudaDriverEntryPointSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+      }
+      get_current = reinterpret_cast<GetCurrent>(f1);
+      get_id = reinterpret_cast<GetId>(f2);
+    }
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
 }
 
 bool encode_bf16_map(CUtensorMap* map, void* base, int rank, const uint64_t* dims,

@@ -25,6 +25,12 @@ bool current_device_info(DeviceInfo* out);
 // cuTensorMapEncodeTiled, resolved once from the driver.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// Unique id (cuCtxGetId) of the calling thread's current CUDA context, or 0
+// if there is none or the driver does not report one.  Ids are never reused
+// within a process, so a cache keyed on it goes stale neither after
+// cudaDeviceReset nor under another context on the same device.
+unsigned long long current_context_id();
+
 // Encode a tiled bf16 tensor map with a 128-, 64- or 32-byte swizzle, or
 // none (swizzle_bytes = 0).
 // dims/strides are innermost first; strides (bytes) exclude dimension 0.

@@ -77,6 +77,9 @@ struct Params {
   float* part;              // [G][m16 / 4][128][4] fp32 partial tiles, one slot per CTA
   unsigned long long* flag; // [G] = epoch once the CTA's partial tile is written
   unsigned long long epoch; // distinct for every launch
+  unsigned long long wait_epoch;   // what a finaliser waits for (epoch, or a stale
+                                   // value under the failure-detection test switch)
+  unsigned long long flag_wait_ns; // limit of one finaliser wait
   int32_t* status;
   int M, N, r;
   int m16;        // tokens rounded up to 16
@@ -389,12 +392,13 @@ inline size_t smem_bytes(int stages, uint32_t stage_bytes) {
   return 1024 + bar_offset(stages, stage_bytes) + kBarBytes;
 }
 
-// Spin (bounded) until *f == v with acquire semantics.
-__device__ bool wait_flag(const unsigned long long* f, unsigned long long v, int32_t* status) {
+// Spin (bounded by limit_ns) until *f == v with acquire semantics.
+__device__ bool wait_flag(const unsigned long long* f, unsigned long long v,
+                          unsigned long long limit_ns, int32_t* status) {
   if (ld_acquire_u64(f) == v) return true;
   const unsigned long long t0 = globaltimer();
   while (ld_acquire_u64(f) != v) {
-    if (globaltimer() - t0 > kWaitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       set_status(status, IDLM_DEV_TIMEOUT);
       return false;
     }
@@ -600,7 +604,7 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
         while (c_hi < static_cast<int>(gridDim.x) && range_begin(p, c_hi) < tile_end) ++c_hi;
         if (et == 0) {
           for (int c = c_lo; c < c_hi; ++c)
-            if (!wait_flag(&p.flag[c], p.epoch, p.status)) {
+            if (!wait_flag(&p.flag[c], p.wait_epoch, p.flag_wait_ns, p.status)) {
               *epi_fail = 1;
               *abort_flag = 1;
               break;
@@ -840,11 +844,12 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
   DeviceInfo dev;
   if (!current_device_info(&dev)) return IDLM_ERR_CUDA;
   static std::mutex mu;
-  static bool done[64] = {};
+  static unsigned long long done[64] = {};
+  const unsigned long long ctx = current_context_id();
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev.device < 0 || dev.device >= 64) return IDLM_ERR_CUDA;
-    if (!done[dev.device]) {
+    if (done[dev.device] != ctx || ctx == 0) {
       if (cudaFuncSetAttribute(lora::lora_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dev.max_smem_optin) != cudaSuccess)
         return IDLM_ERR_CUDA;
@@ -853,7 +858,7 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
       if (cudaFuncSetAttribute(lora::lora_t_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return IDLM_ERR_CUDA;
-      done[dev.device] = true;
+      done[dev.device] = ctx;
     }
   }
   // launches get distinct epochs, so the flags never need clearing
@@ -924,6 +929,13 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
     p.part = reinterpret_cast<float*>(wsb + wl.part);
     p.flag = reinterpret_cast<unsigned long long*>(wsb + wl.flag);
     p.epoch = epoch;
+    // Failure-detection test switch: with IDLM_TEST_STALE_FLAGS=1 a finaliser
+    // waits for a flag value that no CTA writes, so its bounded wait runs out
+    // (after 20 ms) and the call ends with TIMEOUT in the status word.
+    const char* stale = std::getenv("IDLM_TEST_STALE_FLAGS");
+    const bool stale_test = stale && stale[0] == '1';
+    p.wait_epoch = stale_test ? epoch + 1 : epoch;
+    p.flag_wait_ns = stale_test ? 20000000ull : kWaitNs;
     p.status = status;
     p.M = Ms;
     p.N = N;

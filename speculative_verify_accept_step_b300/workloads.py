@@ -31,10 +31,10 @@ synthetic batches stand in for them with the pages' stride N=4 and batch C=64):
                            cached tokens.
 =========================  ====================================================
 
-The noise scale sigma per acceptance target is read from
-``tests/golden/noise_table.json``, written by
+The noise scale sigma per acceptance target is read from ``noise_table.json``
+beside this module (input-generation parameters only), written by
 ``tests/golden/make_noise_table.py`` (a bisection that calls the oracle's
-softmax only).
+softmax only; the script is test infrastructure, the table is data).
 """
 
 import json
@@ -48,7 +48,7 @@ FULL = 1
 FRESH = 0
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-NOISE_TABLE = os.path.join(os.path.dirname(_HERE), "tests", "golden", "noise_table.json")
+NOISE_TABLE = os.path.join(_HERE, "noise_table.json")
 
 
 @dataclass(frozen=True)

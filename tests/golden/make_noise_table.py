@@ -1,4 +1,5 @@
-"""Write noise_table.json: the MASK-logit noise scale per acceptance target.
+"""Write the package's noise_table.json: the MASK-logit noise scale per
+acceptance target (input-generation data that the seeded workloads read).
 
 The synthetic q-logits of a draft are the verifying row's clean logits z plus
 sigma * N(0, 1).  For z ~ N(0, 3^2) over V = 151936 entries (both rows rounded
@@ -48,7 +49,8 @@ def main():
         print(t, table[str(t)], mean_overlap(z, eps, table[str(t)]))
     out = dict(sigma=table, V=V, logit_std=LOGIT_STD, rows=ROWS, seed=SEED,
                note="written by tests/golden/make_noise_table.py")
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "noise_table.json")
+    root = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    path = os.path.join(root, "speculative_verify_accept_step_b300", "noise_table.json")
     with open(path, "w") as f:
         json.dump(out, f, indent=1)
         f.write("\n")

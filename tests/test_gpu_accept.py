@@ -71,7 +71,7 @@ def _small_batch(C, N, V, seed, scale=2.0, noise=0.7, dtype=torch.bfloat16):
                 mode0=torch.zeros(C, dtype=torch.uint8))
 
 
-@pytest.mark.parametrize("N", [2, 3, 8])
+@pytest.mark.parametrize("N", [2, 3, 8, 16])
 def test_other_strides(cuda_device, N):
     b = _small_batch(32, N, 4096, seed=N)
     _check_pair(b, N, 1.0, isd.PROPOSE_ARGMAX, 1, 7)

@@ -61,6 +61,18 @@ def test_ragged_tails_and_row_packings(cuda_device, N):
     assert_attention_close(out, oracle_attention(a))
 
 
+@pytest.mark.parametrize("Hq,N", [(8, 9), (8, 16), (8, 20), (16, 9), (16, 16), (24, 11)])
+def test_more_than_16_rows_per_request(cuda_device, Hq, N):
+    # G = Hq / 8 query heads per kv head; R = 2N - 1 = 17 .. 39 rows per
+    # request, so a unit's new keys span two or three 16-row blocks
+    lens = [0, 1, 15, 16, 40, 257]
+    a, R = _custom(len(lens), N, lens, Hq=Hq, Hkv=8, seed=20 + N, fresh=(2,))
+    assert (Hq // 8) * R <= 64 and R > 16
+    out, st = gpu_attention(a, R)
+    assert st == 0
+    assert_attention_close(out, oracle_attention(a))
+
+
 def test_mixed_fresh_and_full_rows(cuda_device):
     lens = [40, 0, 300, 16]
     a, R = _custom(4, 4, lens, seed=11, fresh=(1, 2))
@@ -82,7 +94,10 @@ def test_headline_workload_full_size(cuda_device):
     out, st = gpu_attention(a, w.rows_full)
     assert st == 0
     assert torch.isfinite(out.float()).all()
-    assert_attention_close(out, oracle_attention(a, requests=[0, 1, 17, 38, 63]))
+    # 16 requests across the batch: at this size every unit is cut by the
+    # balanced split, so these also check the merge of partial results
+    pick = [0, 1, 5, 9, 13, 17, 21, 25, 31, 37, 38, 42, 47, 52, 58, 63]
+    assert_attention_close(out, oracle_attention(a, requests=pick))
 
 
 def test_ragged_workload_sampled_requests(cuda_device):

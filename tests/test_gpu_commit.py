@@ -32,7 +32,7 @@ def _oracle(a, n_commit):
 
 
 @pytest.mark.parametrize("name", ["isd_tiny_c1_n2_f32", "isd_c4_n4_ctx512_2048",
-                                  "isd_c64_n4_ctx1k_32k"])
+                                  "isd_c64_n4_ctx4096", "isd_c64_n4_ctx1k_32k"])
 def test_commit_bit_exact(cuda_device, name):
     w = wl.WORKLOADS[name]
     a = wl.attention_inputs(w)

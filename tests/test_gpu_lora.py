@@ -24,7 +24,7 @@ def f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def gpu_lora(x, w, a, b, g, s, dev="cuda"):
+def gpu_lora_status(x, w, a, b, g, s, dev="cuda"):
     M, K = x.shape
     N, r = w.shape[0], a.shape[0]
     ws = torch.empty(lib.idlm_gated_lora_workspace_size(M, K, N, r), dtype=torch.uint8,
@@ -33,7 +33,12 @@ def gpu_lora(x, w, a, b, g, s, dev="cuda"):
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     lib.idlm_gated_lora(x.to(dev), w.to(dev), a.to(dev), b.to(dev), g.to(dev), s, y, ws, st)
     torch.cuda.synchronize()
-    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    return y, int(st.item())
+
+
+def gpu_lora(x, w, a, b, g, s, dev="cuda"):
+    y, st = gpu_lora_status(x, w, a, b, g, s, dev)
+    assert st == 0, f"device status {st}"
     return y
 
 
@@ -160,3 +165,21 @@ def test_fused_projections_match_the_separate_ones(cuda_device):
     ref = np.array([isd.gated_lora(xs[m:m + 1], wf[n:n + 1], af, bf[n:n + 1], g[m:m + 1],
                                    inp["lora_scale"])[0, 0] for m, n in zip(ms, ns)])
     assert_close(yf[ms, ns], ref)
+
+
+def test_a_wait_that_runs_out_reports_timeout_and_the_context_survives(cuda_device, monkeypatch):
+    """Failure detection without a GPU fault.  Under the test switch
+    IDLM_TEST_STALE_FLAGS=1 a CTA that adds the partial sums of a split tile
+    waits for a flag value that no CTA ever writes; its bounded wait (20 ms)
+    runs out, the kernel records TIMEOUT (5) in the status word, drains its
+    copies, frees its tensor memory and returns.  The next call, without the
+    switch, must run normally and match the oracle."""
+    x, w, a, b, g = case(64, 1024, 256, 16, seed=13)
+    monkeypatch.setenv("IDLM_LORA_GRID", "7")   # 2 tiles x 17 K steps over 7 CTAs: split
+    monkeypatch.setenv("IDLM_TEST_STALE_FLAGS", "1")
+    _, st = gpu_lora_status(x, w, a, b, g, 1.0)
+    assert st == 5, f"expected TIMEOUT, device status {st}"
+    monkeypatch.delenv("IDLM_TEST_STALE_FLAGS")
+    y = gpu_lora(x, w, a, b, g, 1.0)
+    ref = isd.gated_lora(f64(x), f64(w), f64(a), f64(b), g.numpy(), 1.0)
+    assert_close(f64(y), ref)

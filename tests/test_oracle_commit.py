@@ -41,7 +41,11 @@ def test_commit_appends_rows_and_nothing_else():
     for c, L in enumerate(case["seq_lens"]):
         n = n_commit[c]
         assert seq[c] == L + n
-        assert rel[c] == -(-(L + n) // P)
+        # releasable_from: one past the last page-table entry that holds a
+        # committed slot, counted slot by slot (no page holds one: 0)
+        holding = {s // P for s in range(L + n)}
+        assert rel[c] == (max(holding) + 1 if holding else 0)
+        assert all(j in holding for j in range(rel[c]))
         t0 = case["qo_indptr"][c]
         if L:
             assert np.array_equal(_seq(kc, case["page_table"][c], L, P),
@@ -58,6 +62,27 @@ def test_commit_appends_rows_and_nothing_else():
             if (page, off) not in touched:
                 assert np.array_equal(kc[page, :, off], case["k_cache"][page, :, off])
                 assert np.array_equal(vc[page, :, off], case["v_cache"][page, :, off])
+
+
+@pytest.mark.parametrize("lens", [(0, 15, 16, 17), (31, 32, 33, 1)])
+def test_releasable_pages_counted_slot_by_slot(lens):
+    """Every page-table entry before releasable_from holds a committed slot,
+    none from it on: checked against the slots' own page indices."""
+    case = _case(seed=3, lens=lens)
+    P = case["page_size"]
+    for n_commit in ([0, 0, 0, 0], [1, 1, 1, 1], [4, 4, 7, 7]):
+        n_commit = np.minimum(np.array(n_commit), np.diff(case["qo_indptr"]))
+        _, _, seq, rel = kv_commit(case["k_cache"], case["v_cache"], case["page_table"],
+                                   case["seq_lens"], case["k_new"], case["v_new"],
+                                   case["qo_indptr"], n_commit, P)
+        for c in range(len(lens)):
+            used = np.zeros(case["page_table"].shape[1], dtype=bool)
+            for s in range(int(seq[c])):
+                used[s // P] = True
+            free = np.nonzero(~used)[0]
+            first_free = int(free[0]) if free.size else used.size
+            assert rel[c] == first_free
+            assert not used[first_free:].any()
 
 
 def test_zero_commit_keeps_everything():
