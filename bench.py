@@ -30,6 +30,7 @@ import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "ISD accepted tokens/s at C=64,N=4; attention+accept HBM GB/s vs B300 peak"
+LAUNCHES_PER_STEP = 5
 
 
 def parse():
@@ -42,9 +43,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-lora", action="store_true", help="skip the gated-LoRA leg")
-    ap.add_argument("--leg", default="step", choices=["step", "lora"],
+    ap.add_argument("--no-ragged", action="store_true",
+                    help="skip the ragged 1k-32k workload leg")
+    ap.add_argument("--leg", default="step", choices=["step", "lora", "layer"],
                     help="lora: only the gated-LoRA projections (prints their JSON)")
     ap.add_argument("--lora-reps", type=int, default=20)
+    ap.add_argument("--lora-rank", type=int, default=None)
     ap.add_argument("--profile-run", action="store_true",
                     help="few launches for a profiler: no clock sampling, e2e or CPU leg")
     return ap.parse_args()
@@ -59,54 +63,113 @@ def peaks():
     return 6400.0, 1800.0, "fallback"
 
 
-def lora_leg(dev, reps=20, fused=False):
+LORA_LAYER = [("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")),
+              ("down", ("down",))]
+
+
+def lora_leg(dev, reps=20, fused=True, rank=None):
     """The gated-LoRA projections of one decoder layer (workload lora_layer_m448:
     hidden 4096, FFN 12288, 448 token rows, rank 16, gate on at MASK rows),
-    each through idlm_gated_lora, timed alone with CUDA events.  Returns
-    per-projection and whole-layer TFLOP/s (algorithmic 2 M K N per
-    projection; the adapter's extra work is not counted).  fused=True runs
-    the projections that share an input as one call each (q|k|v: N = 6144,
-    rank 48; gate|up: N = 24576, rank 32; B block diagonal), the same layer
-    arithmetic in four calls."""
+    timed alone with CUDA events.  fused=True is the layer's path: the
+    projections that share an input run as one idlm_gated_lora_grouped call
+    each (q|k|v: N = 6144, three adapter groups; gate|up: N = 24576, two),
+    four calls in all; fused=False times the seven projections one call
+    each.  rank overrides the adapters' rank (r = 128 is the pages').
+    Returns per-call and whole-layer TFLOP/s (algorithmic 2 M K N per
+    projection; the adapter's own work is not counted)."""
     import speculative_verify_accept_step_b300 as L
     from speculative_verify_accept_step_b300 import workloads as wl
     w = wl.WORKLOADS["lora_layer_m448"]
-    inp = wl.lora_inputs(w)
+    inp = wl.lora_inputs(w, rank=rank)
     x = inp["x"].to(dev)
     xf = torch.randn(w.T, w.ffn, generator=torch.Generator().manual_seed(3)).bfloat16().to(dev)
     gate = inp["row_gate"].to(dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    groups = ([("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")),
-               ("down", ("down",))] if fused else
-              [(n, (n,)) for n in ("q", "k", "v", "o", "gate", "up", "down")])
+    groups = LORA_LAYER if fused else [(n, (n,)) for n in ("q", "k", "v", "o", "gate", "up", "down")]
     out, tot_flop, tot_ms = {}, 0.0, 0.0
     for name, members in groups:
-        src = wl.fuse_projections(inp["proj"], members) if fused else inp["proj"][name]
-        pj = {k: v.to(dev) for k, v in src.items()}
+        pj = {k: torch.cat([inp["proj"][m][k] for m in members]).to(dev) for k in ("w", "a", "b")}
+        rows = [inp["proj"][m]["w"].shape[0] for m in members]
         xi = xf if name == "down" else x
         M, K = xi.shape
-        N, r = pj["w"].shape[0], pj["a"].shape[0]
-        ws = torch.empty(L.idlm_gated_lora_workspace_size(M, K, N, r), dtype=torch.uint8,
-                         device=dev)
+        N, r = pj["w"].shape[0], pj["a"].shape[0] // len(members)
+        ws = torch.empty(L.idlm_gated_lora_grouped_workspace_size(M, K, N, r, len(members)),
+                         dtype=torch.uint8, device=dev)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def call():
+            L.idlm_gated_lora_grouped(xi, pj["w"], pj["a"], pj["b"], gate, inp["lora_scale"],
+                                      rows, y, ws, st)
         for _ in range(3):
-            L.idlm_gated_lora(xi, pj["w"], pj["a"], pj["b"], gate, inp["lora_scale"], y, ws, st)
+            call()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(reps):
-            L.idlm_gated_lora(xi, pj["w"], pj["a"], pj["b"], gate, inp["lora_scale"], y, ws, st)
+            call()
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps
         fl = 2.0 * M * K * N
         tot_flop += fl
         tot_ms += ms
-        out[name] = {"M": M, "K": K, "N": N, "r": r, "us": ms * 1e3, "TFLOP/s": fl / ms / 1e9}
+        out[name] = {"M": M, "K": K, "N": N, "r": r, "groups": len(members), "us": ms * 1e3,
+                     "TFLOP/s": fl / ms / 1e9}
         del ws, y
     assert int(st.item()) == 0, f"device status {int(st.item())}"
-    return {"workload": w.name, "projections": out, "layer_us": tot_ms * 1e3,
-            "TFLOP/s": tot_flop / tot_ms / 1e9, "launches_per_projection": 2}
+    return {"workload": w.name, "rank": inp["rank"], "calls": out, "layer_us": tot_ms * 1e3,
+            "TFLOP/s": tot_flop / tot_ms / 1e9, "layer_GFLOP": tot_flop / 1e9}
+
+
+def layer_leg(dev, reps=10):
+    """The whole decoder layer of the gated-LoRA workload through
+    idlm_risd_layer (RMSNorm, q|k|v, attention over the 4096-token paged KV,
+    o, residual, RMSNorm, gate|up, SwiGLU, down, residual; 448 rows), timed
+    with CUDA events at adapter rank 0, 16 (the workload) and 128 (the
+    pages'); alpha = time with adapters / time without.  The KV cache and
+    page table are the headline attention batch's."""
+    import speculative_verify_accept_step_b300 as L
+    from speculative_verify_accept_step_b300 import workloads as wl
+    w = wl.WORKLOADS["lora_layer_m448"]
+    res = {"workload": w.name, "rows": w.T}
+    base = None
+    for rank in (0, 16, 128):
+        inp = wl.layer_inputs(w, rank=rank)
+        W = {k: v.to(dev) for k, v in inp["W"].items()}
+        lw = L.layer_weights(W, w.hidden, w.ffn, w.Hq, w.Hkv, w.D, rank, inp["lora_scale"])
+        x = inp["x"].to(dev)
+        M, C = x.shape[0], inp["page_table"].shape[0]
+        ws = torch.empty(L.idlm_risd_layer_workspace_size(lw, M, C, w.page_size, w.rows_full),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(x)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        dv = {k: inp[k].to(dev) for k in ("k_cache", "v_cache", "page_table", "seq_lens",
+                                         "qo_indptr", "row_gate")}
+
+        def call():
+            L.idlm_risd_layer(lw, x, out, dv["row_gate"], dv["k_cache"], dv["v_cache"],
+                              dv["page_table"], dv["seq_lens"], dv["qo_indptr"], w.rows_full,
+                              ws, st)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, f"device status {int(st.item())}"
+        us = e0.elapsed_time(e1) / reps * 1e3
+        res[f"r{rank}_us"] = us
+        if rank == 0:
+            base = us
+        else:
+            res[f"alpha_r{rank}"] = us / base
+        del W, ws, dv, inp
+        torch.cuda.empty_cache()
+    res["alpha_pages"] = 1.12
+    return res
 
 
 def source_hash(name):
@@ -377,18 +440,26 @@ def run_ours(args):
     both_gbs = (a_bytes + c_bytes) / ((att_ms + acc_ms) * 1e-3) / 1e9
 
     e2e = None if args.profile_run else run_e2e(st, args.e2e_steps, ws)
+    ragged = None
+    if not args.profile_run and not args.no_ragged and w.name != "isd_c64_n4_ctx1k_32k":
+        ragged = workload_leg("isd_c64_n4_ctx1k_32k", dev)
     lora = None
     if not args.profile_run and not args.no_lora:
         lora = lora_leg(dev)
-        lora["peak"] = bf16
-        lora["frac"] = lora["TFLOP/s"] / bf16
-        lora["bound"] = "tensor"
-        try:   # the same layer with q|k|v and gate|up fused into one call each
-            lf = lora_leg(dev, fused=True)
-            lora["fused"] = {"layer_us": lf["layer_us"], "TFLOP/s": lf["TFLOP/s"],
-                             "frac": lf["TFLOP/s"] / bf16, "projections": lf["projections"]}
+        lora.update({"peak": bf16, "peak_kind": peak_kind, "frac": lora["TFLOP/s"] / bf16,
+                     "bound": "tensor", "path": "4 grouped calls (q|k|v, o, gate|up, down)"})
+        try:   # the seven projections one call each, for comparison
+            ls = lora_leg(dev, fused=False)
+            lora["separate"] = {"layer_us": ls["layer_us"], "TFLOP/s": ls["TFLOP/s"],
+                                "frac": ls["TFLOP/s"] / bf16, "calls": ls["calls"]}
         except Exception as e:   # reported, never fatal to the step's line
-            lora["fused"] = {"error": str(e)[:300]}
+            lora["separate"] = {"error": str(e)[:300]}
+    layer = None
+    if not args.profile_run and not args.no_lora:
+        try:
+            layer = layer_leg(dev)
+        except Exception as e:   # reported, never fatal to the step's line
+            layer = {"error": str(e)[:300]}
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.profile_run:
         cpu = cpu_baseline(w, st.host)
@@ -428,11 +499,15 @@ def run_ours(args):
         "tokens_per_step": n_out / K,
         "accepted_drafts_per_step": n_acc / K,
         "accepted_drafts_per_s": allreduce(float(n_acc), ws, _sum_op()) / (ms * 1e-3),
-        "gpu_launches": 5 * K,
+        # per step: paged_attn_kernel; vocab_stream_kernel, decide_kernel,
+        # work_kernel; commit_kernel (no memsets or copies)
+        "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "lora": lora,
+        "layer": layer,
+        "workloads": {"isd_c64_n4_ctx1k_32k": ragged} if ragged else None,
     }
     print(json.dumps(line))
 
@@ -450,51 +525,128 @@ def _sum_op():
 def run_e2e(st, K, ws):
     """Same metric through the C ABI with host buffers: every step copies its
     inputs (Q, new K/V rows, logits, layout and draft state) from pinned host
-    memory and reads the emitted tokens back."""
+    memory and reads the emitted tokens back.  The copies of step k+1 run on
+    a copy stream while step k computes (two input buffers), and each step's
+    results go back on a third stream, so the PCIe transfers overlap the
+    kernels; the timed region spans all of it."""
+    L, w = st.L, st.w
     a, b = st.host["a"], st.host["b"]
     pin = lambda t: t.pin_memory()
     h = dict(q=pin(a["q"]), k_new=pin(a["k_new"]), v_new=pin(a["v_new"]),
              logits=pin(b["logits1"]), page_table=pin(a["page_table"]),
-             seq_lens=pin(a["seq_lens"]), qo=pin(a["qo_indptr"]),
+             seq_lens=pin(a["seq_lens"]), qo=pin(a["qo_indptr"]), qo1=pin(b["qo1"]),
              mode=pin(st.mode1.cpu()), drafts=pin(st.drafts.cpu()), dq=pin(st.dq.cpu()),
              prow=pin(st.prow.cpu()))
     h2d = sum(t.numel() * t.element_size() for t in h.values())
-    o = st.outs()
-    back = {k: torch.empty(o[k].shape, dtype=o[k].dtype).pin_memory()
-            for k in ("out_tokens", "n_out", "next_drafts", "next_mode")}
-    d2h = sum(t.numel() * t.element_size() for t in back.values())
-    dev_logits = torch.empty_like(st.logits1)
-    tokens = 0
+    bufs = [{k: torch.empty(t.shape, dtype=t.dtype, device=st.dev) for k, t in h.items()}
+            for _ in range(2)]
+    outs = [st.outs() for _ in range(K)]
+    keys_back = ("out_tokens", "n_out", "next_drafts", "next_mode")
+    back = [{k: torch.empty(outs[0][k].shape, dtype=outs[0][k].dtype).pin_memory()
+             for k in keys_back} for _ in range(K)]
+    d2h = sum(t.numel() * t.element_size() for t in back[0].values())
+    seq_out = torch.empty_like(st.seq_lens)
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+
+    def step(k, base):
+        d, o = bufs[k % 2], outs[k]
+        L.idlm_isd_attention(d["q"], d["k_new"], d["v_new"], st.k_cache, st.v_cache,
+                             d["page_table"], d["seq_lens"], d["qo"], st.out, st.att_ws,
+                             st.status, max_rows=w.rows_full, sm_scale=st.sm_scale)
+        L.idlm_isd_accept(d["logits"], d["qo1"], d["mode"], d["drafts"], d["dq"], st.logits0,
+                          d["prow"], w.N, w.temperature, L.PROPOSE_ARGMAX, 0, base + k,
+                          o["n_accepted"], o["out_tokens"], o["n_out"], o["n_commit"],
+                          o["next_drafts"], o["next_q_stats"], o["next_mode"],
+                          o["next_mask_row0"], st.acc_ws, st.status)
+        L.idlm_kv_commit(st.k_cache, st.v_cache, d["page_table"], d["seq_lens"], seq_out,
+                         d["k_new"], d["v_new"], d["qo"], o["n_commit"], st.status,
+                         releasable_from=st.releasable)
+
+    rate = None
     for rep in range(2):   # one untimed pass, then the timed one
         barrier(ws)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        e0.record(comp)
+        s_in.wait_event(e0)
+        ready, free = [ev(), ev()], [None, None]
+        done = []
         for k in range(K):
-            st.q.copy_(h["q"], non_blocking=True)
-            st.k_new.copy_(h["k_new"], non_blocking=True)
-            st.v_new.copy_(h["v_new"], non_blocking=True)
-            dev_logits.copy_(h["logits"], non_blocking=True)
-            st.page_table.copy_(h["page_table"], non_blocking=True)
-            st.seq_lens.copy_(h["seq_lens"], non_blocking=True)
-            st.qo.copy_(h["qo"], non_blocking=True)
-            st.mode1.copy_(h["mode"], non_blocking=True)
-            st.drafts.copy_(h["drafts"], non_blocking=True)
-            st.dq.copy_(h["dq"], non_blocking=True)
-            st.prow.copy_(h["prow"], non_blocking=True)
-            st.attention()
-            st.accept(o, 30_000_000 + k, logits=dev_logits)
-            st.commit(o)
-            for key, t in back.items():
-                t.copy_(o[key], non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-            if rep:
-                tokens += int(back["n_out"].sum())
-        e1.record()
+            bi = k % 2
+            with torch.cuda.stream(s_in):
+                if free[bi] is not None:
+                    s_in.wait_event(free[bi])
+                for key, t in h.items():
+                    bufs[bi][key].copy_(t, non_blocking=True)
+                ready[bi].record(s_in)
+            comp.wait_event(ready[bi])
+            step(k, 30_000_000 + 1000 * rep)
+            free[bi] = ev()
+            free[bi].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(free[bi])
+                for key in keys_back:
+                    back[k][key].copy_(outs[k][key], non_blocking=True)
+                fin = ev()
+                fin.record(s_out)
+                done.append(fin)
+        comp.wait_event(done[-1])
+        e1.record(comp)
         torch.cuda.synchronize()
-    tokens, ms, rate = aggregate(tokens, e0.elapsed_time(e1), ws)
+        if rep:
+            tokens = sum(int(bk["n_out"].sum()) for bk in back)
+            tokens, ms, rate = aggregate(tokens, e0.elapsed_time(e1), ws)
     return {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K}
+            "d2h_bytes_per_step": d2h, "steps": K,
+            "note": "inputs double-buffered: copy stream for step k+1 overlaps step k"}
+
+
+def workload_leg(name, dev, steps=20):
+    """Attention, accept and commit of another workload (here the ragged
+    1k-32k batch), timed per kernel with CUDA events as in the main loop."""
+    from speculative_verify_accept_step_b300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    st = Step(w, dev, seed=0)
+    outs = [st.outs() for _ in range(steps)]
+    for i in range(3):
+        st.attention()
+        st.accept(outs[0], 40_000_000 + i)
+        st.commit(outs[0])
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for k in range(steps):
+        ev[k][0].record()
+        st.attention()
+        ev[k][1].record()
+        st.accept(outs[k], k + 1)
+        ev[k][2].record()
+        st.commit(outs[k])
+        ev[k][3].record()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
+    att = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    acc = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    com = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
+    tot = sum(e[0].elapsed_time(e[3]) for e in ev) / steps
+    n_out = torch.stack([o["n_out"] for o in outs]).sum().item()
+    n_rej = torch.stack([(o["next_mode"] == 0).sum() for o in outs]).sum().item()
+    hbm, _, _ = peaks()
+    ab = attention_bytes(w, st.host["a"]["seq_lens"])
+    cb = accept_bytes(w, n_rej / steps)
+    L = st.host["a"]["seq_lens"]
+    res = {"workload": name, "steps": steps, "tokens_per_step": n_out / steps,
+           "tokens_per_s": n_out / (tot * steps * 1e-3),
+           "context": {"min": int(L.min()), "max": int(L.max()), "mean": float(L.float().mean())},
+           "attention": {"us": att * 1e3, "GB/s": ab / (att * 1e-3) / 1e9,
+                         "frac": ab / (att * 1e-3) / 1e9 / hbm, "algorithmic_bytes": ab},
+           "accept": {"us": acc * 1e3, "GB/s": cb / (acc * 1e-3) / 1e9,
+                      "frac": cb / (acc * 1e-3) / 1e9 / hbm, "algorithmic_bytes": cb},
+           "commit": {"us": com * 1e3}}
+    del st, outs
+    torch.cuda.empty_cache()
+    return res
 
 
 # ------------------------------------------------------------- CPU baseline
@@ -739,9 +891,12 @@ def main():
     from speculative_verify_accept_step_b300.build import build
     if not os.path.exists(os.path.join(ROOT, "speculative_verify_accept_step_b300", "libidlm.so")):
         build()
+    if args.leg == "layer":
+        print(json.dumps(layer_leg(torch.device("cuda", 0))))
+        return
     if args.leg == "lora":
         dev = torch.device("cuda", 0)
-        out = lora_leg(dev, reps=args.lora_reps)
+        out = lora_leg(dev, reps=args.lora_reps, rank=args.lora_rank)
         _, bf16, kind = peaks()
         out.update({"peak": bf16, "peak_kind": kind, "frac": out["TFLOP/s"] / bf16})
         print(json.dumps(out))

@@ -133,7 +133,8 @@ idlm_status idlm_isd_attention(
  *
  * [IDLM] "Lossless R-ISD": a LoRA adapter is applied only at MASK positions;
  * verify (clean) positions use the base weights alone, so their outputs equal
- * the base model's bit for bit.  [IDLM] speedup panel: R-ISD overhead 1.12.
+ * the base model's bit for bit; the pages' adapter has rank 128.  [IDLM]
+ * speedup panel: R-ISD overhead 1.12.
  *
  *   Y = X W^T + g_row * lora_scale * (X A^T) B^T,   g_row = row_gate[m] != 0
  *
@@ -144,28 +145,27 @@ idlm_status idlm_isd_attention(
  *   row_gate   [M]     uint8  1 at MASK rows, 0 at clean rows
  *   y          [M, N]  bf16   written for every row
  * fp32 accumulation on the tensor cores (tcgen05); the adapter enters the
- * same accumulation as one more K step, so rows with row_gate = 0 come out
- * bit-identical to the projection with lora_b = 0.  Requirements: K % 8 == 0,
- * r % 8 == 0, 8 <= r <= 64, 16-byte aligned x, w, lora_a, lora_b; any M
- * (token rows run in slices of 448).  Workspace:
- * idlm_gated_lora_workspace_size() bytes, 256-byte aligned (the adapter
- * operands, and fp32 partial tiles with one flag per SM for the split of the
- * K sum); its contents need no initialisation, and one workspace must not be
- * used by two calls at once.  The size depends on the current device.
- * The call launches two kernels per slice of 448 token rows (the adapter's
- * X A^T product, then the GEMM as its programmatic dependent).  The GEMM is
- * a persistent grid of at most one CTA per SM that splits the (tile, K
- * step) work evenly; where a tile's K sum is split, its partial sums are
- * added in a fixed order, so results are reproducible on a given device.
- * A CTA that adds partial sums waits for the CTAs that produce them, so the
- * grid relies on all its CTAs becoming resident: work from other streams
- * that holds SMs for more than 2 s ends the call with TIMEOUT.
+ * same accumulation as one (r <= 64) or two (r <= 128) more K steps, so rows
+ * with row_gate = 0 come out bit-identical to the projection with
+ * lora_b = 0.  Requirements: K % 8 == 0, r % 8 == 0, 0 <= r <= 128 (r = 0:
+ * no adapter; lora_a, lora_b and row_gate may then be NULL), 16-byte aligned
+ * x, w, lora_a, lora_b; any M (token rows run in slices of 448).
+ * Workspace: idlm_gated_lora_workspace_size() bytes, 256-byte aligned (the
+ * adapter operands T = g s X A^T and, where r % 64 != 0, B padded to 64
+ * columns; fp32 partial tiles, two slots per SM); its contents need no
+ * initialisation, and one workspace must not be used by two calls at once.
+ * The size depends on the current device.
+ * The call launches per slice of 448 token rows: the adapter kernel
+ * (T = g s X A^T), the GEMM (a persistent grid of at most one CTA per SM
+ * holding whole weight-row tiles and an even share of the K steps of the
+ * tiles left over) and, when a tile's K sum was split, a fix-up kernel that
+ * adds its fp32 partial tiles in a fixed order.  No CTA waits for another,
+ * and results are reproducible on a given device.
  * The environment variable IDLM_LORA_GRID, if set, fixes the grid size
  * (capped at the SMs).  Device errors: TIMEOUT.  Failure-detection test
- * switch: with IDLM_TEST_STALE_FLAGS=1 in the environment, a CTA that adds
- * partial sums waits (for 20 ms) for a flag value that is never written, so
- * any call whose grid splits a tile's K sum ends with TIMEOUT in `status`
- * and leaves that tile's Y unwritten; the call still returns normally and
+ * switch: with IDLM_TEST_STALL=1 in the environment, every GEMM CTA first
+ * waits (for 20 ms) on a barrier that nothing arrives on, so the call ends
+ * with TIMEOUT in `status` and Y unspecified; it still returns normally and
  * the CUDA context stays usable.
  * ---------------------------------------------------------------------- */
 size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r);
@@ -173,6 +173,22 @@ size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r);
 idlm_status idlm_gated_lora(
     const void* x, const void* w, const void* lora_a, const void* lora_b,
     const uint8_t* row_gate, float lora_scale, int M, int K, int N, int r, void* y,
+    void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* Several gated-LoRA projections that share the input X (q|k|v, gate|up) as
+ * one call: the weights are stacked along N, group g owning weight rows
+ * [sum_{h<g} group_rows[h], sum_{h<=g} group_rows[h]) (group_rows is a HOST
+ * array of ngroups entries, each a multiple of 128 except the last, summing
+ * to N); lora_a stacks the groups' adapters, [ngroups * r, K]; lora_b is
+ * [N, r], row n holding the B row of n's group.  Y = X W^T plus, for the
+ * rows of group g, g_row * lora_scale * (X A_g^T) B_g^T.  1 <= ngroups <= 4;
+ * otherwise as idlm_gated_lora, with its own workspace query. */
+size_t idlm_gated_lora_grouped_workspace_size(int M, int K, int N, int r, int ngroups);
+
+idlm_status idlm_gated_lora_grouped(
+    const void* x, const void* w, const void* lora_a, const void* lora_b,
+    const uint8_t* row_gate, float lora_scale, int M, int K, int N, int r,
+    int ngroups, const int* group_rows, void* y,
     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
@@ -195,7 +211,11 @@ idlm_status idlm_gated_lora(
  * SAMPLE-mode proposal of MASK row k (index k-1).  Proposals: argmax of each
  * MASK row (lowest index on ties) or a draw from its q (SAMPLE).
  *
- *   logits         [T, V] (dtype)          this step's output rows
+ *   logits         [T, V] (dtype)          this step's output rows; T is the
+ *                                          buffer's capacity: rows from
+ *                                          qo_indptr[C] on are not read, so a
+ *                                          fixed-shape loop may pass its
+ *                                          largest row count every step
  *   qo_indptr      [C+1] int32
  *   mode           [C] uint8               IDLM_MODE_FULL / IDLM_MODE_FRESH
  *   drafts         [C, N-1] int32          read for FULL requests
@@ -218,7 +238,7 @@ idlm_status idlm_gated_lora(
  *                           sum_v exp(x_v/T - m)) of each MASK row
  *   next_mode      uint8    FULL if nothing was rejected, else FRESH
  *   next_mask_row0 int32    qo_indptr[c] + (number of clean rows)
- *   row_stats      [T, 2] float or NULL: (m, S) of every row
+ *   row_stats      [T, 2] float or NULL: (m, S) of every row in use
  *   dbg            [C, N-1, 4] float or NULL: (u_i, p_i(d_i), q_i(d_i),
  *                           ratio) per draft of FULL requests
  * Requirements: V % 8 == 0, 2 <= N <= 16, temperature >= 0.
@@ -307,6 +327,135 @@ idlm_status idlm_kv_commit(
     const void* k_new, const void* v_new, const int32_t* qo_indptr,
     const int32_t* n_commit, int C, int T, int Hkv, int D, int page_size,
     int num_pages, int dtype, int32_t* releasable_from, int32_t* status,
+    void* stream);
+
+/* ------------------------------------------------------------------------
+ * One R-ISD decoder layer over the step's rows.
+ *
+ * [IDLM] "Lossless R-ISD": LoRA adapters (rank 128 on the pages) act only at
+ * MASK positions, so clean positions reproduce the base model; "Training":
+ * strict causal attention.  The pages do not spell the layer out; this is
+ * the pre-norm layout of the Qwen3-style base models they convert (no rotary
+ * embedding or QK-norm inside the step, as for idlm_isd_attention):
+ *   n1 = RMSNorm(x); [q|k|v] = n1 Wqkv^T (+ gated LoRA per group);
+ *   a = attention(q, k, v) over the paged cache (idlm_isd_attention);
+ *   h = x + a Wo^T (+ gated LoRA); n2 = RMSNorm(h);
+ *   [g|u] = n2 Wgu^T (+ gated LoRA per group);
+ *   out = h + (silu(g) * u) Wd^T (+ gated LoRA)
+ * with RMSNorm(v) = v / sqrt(mean(v^2) + rms_eps) * weight.  Activations
+ * are stored in bf16 between the kernels (fp32 accumulation and elementwise
+ * arithmetic).  Because the step's rows are laid out [clean..., MASK...] per
+ * request and attention is causal, clean rows never see a MASK row, so with
+ * any adapters their outputs equal those of the layer with rank 0 bit for
+ * bit.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int hidden, ffn, n_heads, n_kv_heads, head_dim;
+  int rank;                /* adapter rank, 0 (no adapters) or 8 .. 128, % 8 */
+  float lora_scale, rms_eps;
+  const void* w_qkv;       /* [(Hq + 2 Hkv) D, hidden] bf16: q rows, k rows, v rows */
+  const void* a_qkv;       /* [3 rank, hidden]: the q, k, v adapters' A stacked */
+  const void* b_qkv;       /* [(Hq + 2 Hkv) D, rank] */
+  const void* w_o;         /* [hidden, Hq D] */
+  const void* a_o;         /* [rank, Hq D] */
+  const void* b_o;         /* [hidden, rank] */
+  const void* w_gu;        /* [2 ffn, hidden]: gate rows, then up rows */
+  const void* a_gu;        /* [2 rank, hidden] */
+  const void* b_gu;        /* [2 ffn, rank] */
+  const void* w_down;      /* [hidden, ffn] */
+  const void* a_down;      /* [rank, ffn] */
+  const void* b_down;      /* [hidden, rank] */
+  const void* norm1;       /* [hidden] bf16, or NULL for weight 1 */
+  const void* norm2;       /* [hidden] bf16, or NULL */
+} idlm_layer_weights;
+
+/* Workspace of idlm_risd_layer (the activations, one gated-LoRA workspace
+ * and one attention workspace); 0 for an unsupported shape.  Shapes:
+ * hidden % 8 == 0, ffn % 128 == 0, Hq D and Hkv D multiples of 128. */
+size_t idlm_risd_layer_workspace_size(const idlm_layer_weights* weights, int M, int C,
+                                      int page_size, int max_rows);
+
+/*   x, out        [M, hidden] bf16 (16-byte aligned), M = qo_indptr[C]
+ *   row_gate      [M] uint8  1 at MASK rows
+ *   k_cache .. max_rows   the paged cache and layout, as for
+ *                 idlm_isd_attention (the layer does not write the cache)
+ *   k_new_out, v_new_out  [M, Hkv, D] bf16 or NULL: the step's keys and
+ *                 values, for idlm_kv_commit afterwards
+ * Launches the kernels of the layer in stream order (about 14 launches);
+ * device errors as for idlm_isd_attention and idlm_gated_lora. */
+idlm_status idlm_risd_layer(
+    const idlm_layer_weights* weights, const void* x, void* out, int M,
+    const uint8_t* row_gate, const void* k_cache, const void* v_cache,
+    const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+    const int32_t* qo_indptr, int C, int page_size, int num_pages, int max_rows,
+    void* k_new_out, void* v_new_out, void* workspace, size_t workspace_bytes,
+    int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Stationary-batch decode loop: the hand-off between two steps.
+ *
+ * [IDLM] "Serving (SGLang)": the batch keeps its shape from step to step
+ * (stationary-batch decode loop) and the step is replayed from a CUDA graph;
+ * the abstract names a stationary-batch scheduler.  From this step's accept
+ * and commit results, writes the next step's row layout and row inputs:
+ *   FULL  (next_mode 1): rows [anchor, d_1 .. d_{N-1}, MASK x (N-1)]
+ *   FRESH (next_mode 0): rows [anchor, MASK x (N-1)]
+ * at positions L .. L + rows - 1, where L = seq_lens[c] (after the commit),
+ * the anchor is the last token the step emitted (out_tokens[c][n_out-1], not
+ * yet in the cache) and d_k = next_drafts[c][k-1].
+ *
+ *   mode          [C] uint8 or NULL   this step's modes (counters only)
+ *   next_mode, out_tokens [C, N], n_out, n_accepted (or NULL), next_drafts
+ *                 [C, N-1]            as written by idlm_isd_accept
+ *   seq_lens      [C] int32           committed lengths after idlm_kv_commit
+ *   qo_indptr     [C+1] int32         out: the next step's row layout
+ *   row_req, row_pos, row_token [T] int32   out: request, absolute position
+ *                 and input token of each row (-1 at MASK rows); rows from
+ *                 qo_indptr[C] to T get request 0, position 0, token -2
+ *   counters      [4, C] int32 or NULL   in/out, when count != 0: tokens
+ *                 emitted, forwards, accepted drafts, drafts tested
+ *   history       [C, hist_cap] int32 or NULL   in/out, when count != 0:
+ *                 emitted tokens appended at hist_len[c] (dropped past
+ *                 hist_cap); hist_len [C] int32 in/out
+ *   count         0 for a loop's first layout (nothing to count), else 1
+ * Requirements: 2 <= N <= 16, T >= C (2N - 1).  Device errors: BAD_LAYOUT
+ * (n_out outside [1, N], a negative length).  One kernel launch.
+ * ---------------------------------------------------------------------- */
+idlm_status idlm_isd_advance(
+    int C, int N, int T, const uint8_t* mode, const uint8_t* next_mode,
+    const int32_t* out_tokens, const int32_t* n_out, const int32_t* n_accepted,
+    const int32_t* next_drafts, const int32_t* seq_lens, int32_t* qo_indptr,
+    int32_t* row_req, int32_t* row_pos, int32_t* row_token, int32_t* counters,
+    int32_t* history, int hist_cap, int32_t* hist_len, int count,
+    int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Synthetic logit rows: the seeded workloads' stand-in for the model's
+ * forward pass in a decode loop (not part of the ISD step).
+ *
+ * Row i (i < qo_indptr[C]) of request c = row_req[i] at position
+ * row_pos[i] predicts slot s = row_pos[i] + 1 ([IDLM] "Training": logit
+ * shift).  A clean row (row_token[i] >= 0) holds z(c, s); a MASK row holds
+ * z(c, s) + e(c, s, step) scaled per request, so a draft proposed at one step
+ * is verified against z(c, s) at the next.  Each value is an Irwin-Hall sum
+ * of the eight 16-bit halves of one Philox4x32-10 output (Salmon et al.,
+ * SC'11; counter (v, s, c, d), key (seed, 0x1D1A7E5D), d = 0 for z and
+ * 1 + step for e), centred (minus 4 * 65535), converted exactly to fp32 and
+ * multiplied by scale_z (z) or scale_e[c] (e), the sum rounded to nearest in
+ * fp32 and then to nearest-even in bf16.  A CPU implementation of this
+ * definition reproduces every bit.
+ *
+ *   logits    [T, V] bf16, 16-byte aligned, V % 8 == 0 (rows in use written)
+ *   qo_indptr [C+1], row_req, row_pos, row_token [T] int32 (as
+ *             idlm_isd_advance writes them)
+ *   scale_e   [C] float
+ *   step      < 2^32 - 1
+ * One kernel launch.
+ * ---------------------------------------------------------------------- */
+idlm_status idlm_synth_logits(
+    void* logits, int C, int T, int V, const int32_t* qo_indptr,
+    const int32_t* row_req, const int32_t* row_pos, const int32_t* row_token,
+    float scale_z, const float* scale_e, uint32_t seed, uint32_t step,
     void* stream);
 
 #ifdef __cplusplus

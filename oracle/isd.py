@@ -393,6 +393,94 @@ def gated_lora(x, w, lora_a, lora_b, row_gate, lora_scale):
     return base + t @ np.asarray(lora_b, dtype=np.float64).T
 
 
+def gated_lora_grouped(x, w, lora_a, lora_b, row_gate, lora_scale, group_rows):
+    """Several gated-LoRA projections of one input with stacked weights.
+
+    Group g owns weight rows [sum(group_rows[:g]), sum(group_rows[:g+1]));
+    lora_a stacks the groups' A matrices ([ngroups * r, K]) and lora_b holds
+    each weight row's B row ([N, r]).  Each group is gated_lora with its own
+    A and B; the outputs sit side by side along N.
+    """
+    ng = len(group_rows)
+    r = np.asarray(lora_a).shape[0] // ng
+    outs, n0 = [], 0
+    for g, n in enumerate(group_rows):
+        outs.append(gated_lora(x, np.asarray(w)[n0:n0 + n], np.asarray(lora_a)[g * r:(g + 1) * r],
+                               np.asarray(lora_b)[n0:n0 + n], row_gate, lora_scale))
+        n0 += n
+    return np.concatenate(outs, axis=1)
+
+
+# ---------------------------------------------------------------------------
+# One R-ISD decoder layer ([IDLM] "Lossless R-ISD"; pre-norm layout of the
+# Qwen3-style base models the pages convert -- the pages do not spell the
+# layer out)
+# ---------------------------------------------------------------------------
+
+def round_bf16(x):
+    """Nearest bfloat16 of each value (through float32, ties to even)."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def rmsnorm(x, eps, weight=None):
+    """x / sqrt(mean(x^2) + eps) * weight along the last axis (weight 1 if None)."""
+    x = np.asarray(x, dtype=np.float64)
+    y = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return y if weight is None else y * np.asarray(weight, dtype=np.float64)
+
+
+def silu(x):
+    """x * sigmoid(x) = x / (1 + exp(-x))."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def risd_layer(x, W, row_gate, lora_scale, eps, n_heads, n_kv_heads, head_dim,
+               k_cache, v_cache, page_table, seq_lens, qo_indptr, page_size, store=None):
+    """One decoder layer over the step's rows, gated LoRA at MASK rows.
+
+    W: dict with w_qkv [(Hq+2Hkv)D, H], a_qkv [3r, H], b_qkv [(Hq+2Hkv)D, r],
+    w_o [H, Hq D], a_o, b_o, w_gu [2F, H] (gate rows, then up rows), a_gu
+    [2r, H], b_gu, w_down [H, F], a_down, b_down, norm1, norm2 ([H] or None);
+    rank 0 means no adapters (a_* of zero rows).  store: the rounding applied
+    where an implementation stores an activation (None: exact float64).
+
+        n1 = RMSNorm(x)               h  = x + a Wo^T (+ LoRA)
+        [q|k|v] = n1 Wqkv^T (+ LoRA)  n2 = RMSNorm(h)
+        a = isd_attention(q, k, v)    [g|u] = n2 Wgu^T (+ LoRA)
+                                      out = h + (silu(g) * u) Wd^T (+ LoRA)
+    Returns (out, k_new, v_new).
+    """
+    st = store or (lambda a: a)
+    x = np.asarray(x, dtype=np.float64)
+    T, H = x.shape
+    nq, nkv = n_heads * head_dim, n_kv_heads * head_dim
+    F = np.asarray(W["w_gu"]).shape[0] // 2
+
+    def proj(inp, w, a, b, rows):
+        if np.asarray(a).shape[0] == 0:
+            return np.asarray(inp, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+        return gated_lora_grouped(inp, w, a, b, row_gate, lora_scale, rows)
+
+    n1 = st(rmsnorm(x, eps, W.get("norm1")))
+    qkv = st(proj(n1, W["w_qkv"], W["a_qkv"], W["b_qkv"], [nq, nkv, nkv]))
+    q = qkv[:, :nq].reshape(T, n_heads, head_dim)
+    k_new = qkv[:, nq:nq + nkv].reshape(T, n_kv_heads, head_dim)
+    v_new = qkv[:, nq + nkv:].reshape(T, n_kv_heads, head_dim)
+    a = st(isd_attention(q, k_new, v_new, k_cache, v_cache, page_table, seq_lens, qo_indptr,
+                         page_size, 1.0 / np.sqrt(head_dim)).reshape(T, nq))
+    o = st(proj(a, W["w_o"], W["a_o"], W["b_o"], [H]))
+    h = st(x + o)
+    n2 = st(rmsnorm(h, eps, W.get("norm2")))
+    gu = st(proj(n2, W["w_gu"], W["a_gu"], W["b_gu"], [F, F]))
+    act = st(silu(gu[:, :F]) * gu[:, F:])
+    d = st(proj(act, W["w_down"], W["a_down"], W["b_down"], [H]))
+    return st(h + d), k_new, v_new
+
+
 # ---------------------------------------------------------------------------
 # Closed forms of the pages
 # ---------------------------------------------------------------------------
@@ -424,16 +512,21 @@ MASK_TOKEN = -1
 
 
 def isd_decode(model, first_token, N, n_steps, temperature, proposal_mode,
-               seed, step0=0):
+               seed, step0=0, start_len=None, with_positions=False):
     """Run n_steps ISD steps for a batch of requests from FRESH.
 
     model(row_tok, row_req, row_mask_k, row_last_clean) -> logits [T, V]:
         row_tok is the input token of each row (MASK_TOKEN at MASK rows),
         row_req its request, row_mask_k the MASK offset k = 1..N-1 (0 at
         clean rows) and row_last_clean the input token of the request's last
-        clean row in this step.
+        clean row in this step.  With with_positions=True the model also
+        receives row_pos, the absolute position of each row: the request's
+        committed length L plus the row's offset in its block (the rows sit
+        at L .. L + rows - 1; the module docstring's layout).
     first_token: [C] the token each request starts from (the end of its
         prompt, not yet in the cache).
+    start_len: [C] committed lengths at the start (default 0); every step
+        adds its n_commit.
     Returns (emitted [C, N*n_steps] padded with -1, n_emitted [C],
     per_step [n_steps, C] tokens emitted by each step).
     """
@@ -448,6 +541,8 @@ def isd_decode(model, first_token, N, n_steps, temperature, proposal_mode,
     emitted = np.full((C, N * n_steps), -1, dtype=np.int64)
     n_emitted = np.zeros(C, dtype=np.int64)
     per_step = np.zeros((n_steps, C), dtype=np.int64)
+    length = (np.zeros(C, dtype=np.int64) if start_len is None
+              else np.asarray(start_len).astype(np.int64).copy())
     for s in range(n_steps):
         n_rows = rows_per_request(mode, N)
         qo = np.concatenate([[0], np.cumsum(n_rows)])
@@ -463,7 +558,10 @@ def isd_decode(model, first_token, N, n_steps, temperature, proposal_mode,
         row_mask_k = np.where(is_mask, pos - ncl + 1, 0)
         last_clean = np.where(mode == FULL, drafts[:, M - 1], pending)
         row_last_clean = last_clean[row_req]
-        logits = model(row_tok, row_req, row_mask_k, row_last_clean)
+        if with_positions:
+            logits = model(row_tok, row_req, row_mask_k, row_last_clean, length[row_req] + pos)
+        else:
+            logits = model(row_tok, row_req, row_mask_k, row_last_clean)
         if prev_logits is None:
             prev_logits = np.zeros((1, logits.shape[1]))
         out = isd_accept(logits, qo, mode, drafts, prev_logits, prev_mask_row0,
@@ -478,4 +576,5 @@ def isd_decode(model, first_token, N, n_steps, temperature, proposal_mode,
         mode = out["next_mode"]
         prev_logits = logits
         prev_mask_row0 = out["next_mask_row0"]
+        length += out["n_commit"]
     return emitted, n_emitted, per_step

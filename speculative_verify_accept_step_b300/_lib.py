@@ -31,6 +31,16 @@ class IDLMError(RuntimeError):
     pass
 
 
+class LayerWeights(ctypes.Structure):
+    """idlm_layer_weights (include/idlm.h)."""
+    _fields_ = [("hidden", ctypes.c_int), ("ffn", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("rank", ctypes.c_int),
+                ("lora_scale", ctypes.c_float), ("rms_eps", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in ("w_qkv", "a_qkv", "b_qkv", "w_o", "a_o", "b_o", "w_gu",
+                                       "a_gu", "b_gu", "w_down", "a_down", "b_down", "norm1",
+                                       "norm2")]
+
+
 def lib():
     """Load libidlm.so (raises if it was not built)."""
     global _lib
@@ -64,6 +74,22 @@ def lib():
         L.idlm_gated_lora_workspace_size.argtypes = [i32] * 4
         L.idlm_gated_lora.restype = i32
         L.idlm_gated_lora.argtypes = [vp] * 5 + [f32] + [i32] * 4 + [vp, vp, sz, vp, vp]
+        L.idlm_gated_lora_grouped_workspace_size.restype = sz
+        L.idlm_gated_lora_grouped_workspace_size.argtypes = [i32] * 5
+        L.idlm_gated_lora_grouped.restype = i32
+        L.idlm_gated_lora_grouped.argtypes = ([vp] * 5 + [f32] + [i32] * 5
+                                              + [ctypes.POINTER(ctypes.c_int), vp, vp, sz, vp, vp])
+        L.idlm_synth_logits.restype = i32
+        L.idlm_synth_logits.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, f32, vp,
+                                        ctypes.c_uint32, ctypes.c_uint32, vp]
+        L.idlm_isd_advance.restype = i32
+        L.idlm_isd_advance.argtypes = ([i32, i32, i32] + [vp] * 11 + [vp, vp, i32, vp, i32, vp,
+                                                                      vp])
+        L.idlm_risd_layer_workspace_size.restype = sz
+        L.idlm_risd_layer_workspace_size.argtypes = [ctypes.POINTER(LayerWeights)] + [i32] * 4
+        L.idlm_risd_layer.restype = i32
+        L.idlm_risd_layer.argtypes = ([ctypes.POINTER(LayerWeights), vp, vp, i32, vp, vp, vp, vp,
+                                       i32, vp, vp] + [i32] * 4 + [vp, vp, vp, sz, vp, vp])
         L.idlm_kv_commit.restype = i32
         L.idlm_kv_commit.argtypes = ([vp, vp, vp, i32, vp, vp, vp, vp, vp, vp] + [i32] * 7
                                      + [vp, vp, vp])
@@ -193,6 +219,26 @@ def idlm_gated_lora(x, w, lora_a, lora_b, row_gate, lora_scale, y, workspace, st
     _check(rc, "idlm_gated_lora")
 
 
+def idlm_gated_lora_grouped_workspace_size(M, K, N, r, ngroups):
+    return int(lib().idlm_gated_lora_grouped_workspace_size(M, K, N, r, ngroups))
+
+
+def idlm_gated_lora_grouped(x, w, lora_a, lora_b, row_gate, lora_scale, group_rows, y, workspace,
+                            status, stream=None):
+    """group_rows: the weight rows of each group (a host list of ints)."""
+    _contig(x, w, lora_a, lora_b, row_gate, y, workspace)
+    M, K = x.shape
+    N = w.shape[0]
+    ng = len(group_rows)
+    r = lora_a.shape[0] // ng
+    rows = (ctypes.c_int * ng)(*[int(v) for v in group_rows])
+    rc = lib().idlm_gated_lora_grouped(
+        _ptr(x), _ptr(w), _ptr(lora_a), _ptr(lora_b), _ptr(row_gate), float(lora_scale), M, K,
+        N, r, ng, rows, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _check(rc, "idlm_gated_lora_grouped")
+
+
 # --------------------------------------------------------------------- commit
 
 def idlm_kv_commit(k_cache, v_cache, page_table, seq_lens_in, seq_lens_out, k_new, v_new,
@@ -208,3 +254,69 @@ def idlm_kv_commit(k_cache, v_cache, page_table, seq_lens_in, seq_lens_out, k_ne
         D, page_size, num_pages, _dtype(k_cache), _ptr(releasable_from), _ptr(status),
         _stream(stream))
     _check(rc, "idlm_kv_commit")
+
+
+# ------------------------------------------------------- multi-step loop pieces
+
+def idlm_synth_logits(logits, qo_indptr, row_req, row_pos, row_token, scale_z, scale_e, seed,
+                      step, stream=None):
+    """Synthetic model rows (the seeded workload's stand-in for the forward
+    pass) into logits [T, V] bf16 for the rows in use."""
+    _contig(logits, qo_indptr, row_req, row_pos, row_token, scale_e)
+    T, V = logits.shape
+    C = scale_e.shape[0]
+    rc = lib().idlm_synth_logits(_ptr(logits), C, T, V, _ptr(qo_indptr), _ptr(row_req),
+                                 _ptr(row_pos), _ptr(row_token), float(scale_z), _ptr(scale_e),
+                                 int(seed) & 0xFFFFFFFF, int(step), _stream(stream))
+    _check(rc, "idlm_synth_logits")
+
+
+def idlm_isd_advance(N, mode, next_mode, out_tokens, n_out, n_accepted, next_drafts, seq_lens,
+                     qo_indptr, row_req, row_pos, row_token, status, counters=None,
+                     history=None, hist_len=None, count=True, stream=None):
+    _contig(mode, next_mode, out_tokens, n_out, n_accepted, next_drafts, seq_lens, qo_indptr,
+            row_req, row_pos, row_token, counters, history, hist_len)
+    C = next_mode.shape[0]
+    T = row_req.shape[0]
+    cap = 0 if history is None else history.shape[1]
+    rc = lib().idlm_isd_advance(C, N, T, _ptr(mode), _ptr(next_mode), _ptr(out_tokens),
+                                _ptr(n_out), _ptr(n_accepted), _ptr(next_drafts), _ptr(seq_lens),
+                                _ptr(qo_indptr), _ptr(row_req), _ptr(row_pos), _ptr(row_token),
+                                _ptr(counters), _ptr(history), cap, _ptr(hist_len),
+                                1 if count else 0, _ptr(status), _stream(stream))
+    _check(rc, "idlm_isd_advance")
+
+
+# ------------------------------------------------------------- decoder layer
+
+def layer_weights(W, hidden, ffn, n_heads, n_kv_heads, head_dim, rank, lora_scale=1.0,
+                  rms_eps=1e-6):
+    """idlm_layer_weights over a dict of device tensors (keys as in the
+    struct; a_* / b_* / norm* may be missing).  The dict must outlive the
+    struct."""
+    lw = LayerWeights(hidden, ffn, n_heads, n_kv_heads, head_dim, rank, lora_scale, rms_eps)
+    for name, _ in LayerWeights._fields_[8:]:
+        t = W.get(name)
+        if t is not None:
+            _contig(t)
+            setattr(lw, name, t.data_ptr())
+    return lw
+
+
+def idlm_risd_layer_workspace_size(lw, M, C, page_size, max_rows):
+    return int(lib().idlm_risd_layer_workspace_size(ctypes.byref(lw), M, C, page_size, max_rows))
+
+
+def idlm_risd_layer(lw, x, out, row_gate, k_cache, v_cache, page_table, seq_lens, qo_indptr,
+                    max_rows, workspace, status, k_new_out=None, v_new_out=None, stream=None):
+    _contig(x, out, row_gate, k_cache, v_cache, page_table, seq_lens, qo_indptr, workspace,
+            k_new_out, v_new_out)
+    M = x.shape[0]
+    num_pages, _, page_size, _ = k_cache.shape
+    C, max_pages = page_table.shape
+    rc = lib().idlm_risd_layer(
+        ctypes.byref(lw), _ptr(x), _ptr(out), M, _ptr(row_gate), _ptr(k_cache), _ptr(v_cache),
+        _ptr(page_table), max_pages, _ptr(seq_lens), _ptr(qo_indptr), C, page_size, num_pages,
+        max_rows, _ptr(k_new_out), _ptr(v_new_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    _check(rc, "idlm_risd_layer")

@@ -13,7 +13,8 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libidlm.so")
-SOURCES = ["host_util.cu", "attention.cu", "accept.cu", "commit.cu", "lora.cu"]
+SOURCES = ["host_util.cu", "attention.cu", "accept.cu", "commit.cu", "lora.cu", "synth.cu",
+           "advance.cu", "layer.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -413,7 +413,10 @@ __global__ void __launch_bounds__(kK1Threads, 1) vocab_stream_kernel(const Param
   __syncthreads();
   griddep_launch_dependents();
 
-  const long long W = static_cast<long long>(p.T) * p.CH;
+  // rows in use: qo_indptr[C] (T is the capacity of the logits buffer, so a
+  // fixed-shape loop can pass its largest row count every step)
+  const int T_used = min(max(__ldg(p.qo + p.C), 0), p.T);
+  const long long W = static_cast<long long>(T_used) * p.CH;
   const long long lo = W * blockIdx.x / gridDim.x;
   const long long hi = W * (blockIdx.x + 1) / gridDim.x;
   const int n = static_cast<int>(hi - lo);

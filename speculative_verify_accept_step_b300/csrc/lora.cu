@@ -4,49 +4,46 @@
 // Source: "Introspective Diffusion Language Models" (project page), section
 // "Lossless R-ISD" (a LoRA adapter applied only at MASK positions; verify
 // positions keep the base weights, so their outputs equal the base model's
-// bit for bit) and the speedup panel (R-ISD overhead alpha = 1.12).
+// bit for bit; rank 128) and the speedup panel (R-ISD overhead alpha = 1.12).
 //
 // The step's token rows are few (M = C (2N - 1) = 448 at C = 64, N = 4) and
-// the weights are large (N x K up to 12288 x 4096), so the tensor-core tile
-// puts the weight rows on the MMA's M side and the tokens on its N side:
-// one CTA accumulates a [128 weight rows x M tokens] tile of Y^T in tensor
-// memory (up to 448 tokens per launch: two MMAs of N <= 256 per K step in
-// 512 TMEM columns), reading each weight byte once from HBM while X stays in L2.
+// the weights are large (N x K up to 24576 x 4096), so the tensor-core tile
+// puts the weight rows on the MMA's M side and the tokens on its N side: one
+// CTA accumulates a [128 weight rows x M tokens] tile of Y^T in tensor memory
+// (up to 448 tokens per launch: two MMAs of N <= 256 per K step in 512 TMEM
+// columns), reading each weight byte once from HBM while X stays in L2.
 //
-// The LoRA term is one more K step of the same accumulation: the operands
-// of that step are B (the weight side, [N x r]) and T = g s X A^T (the token
-// side, [M x r]), both copied to the workspace as rows of 64 values (zeros
-// past r) so they load like any other K block.  Rows with g = 0 have T = 0,
-// which adds exact zeros to their fp32 accumulators: their outputs are
-// bit-identical to the base projection computed by this kernel without the
-// adapter.
+// The LoRA term is one or two more K steps of the same accumulation (rank r
+// <= 64 or <= 128): their operands are B (the weight side, [N x r]) and
+// T = g s X A^T (the token side, [M x r]), both kept as rows of 64-value
+// blocks (zeros past r) so that they load like any other K block.  Rows with
+// g = 0 have T = 0, which adds exact zeros to their fp32 accumulators: their
+// outputs are bit-identical to the base projection computed by this kernel
+// without the adapter.  Several projections that share the input (q|k|v,
+// gate|up) run as one call with weights stacked along N and one adapter per
+// group of weight rows: a tile's adapter steps read its group's T columns.
 //
-// Kernels:
-//   lora_t_kernel     T = g s X A^T with mma.sync (fp32 accumulation, K
-//                     split over CTAs, summed in a fixed order), stored as
-//                     bf16 (a [M x r] product, 0.03% of the flops), and B
-//                     padded to 64 columns.
-//   lora_gemm_kernel  tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in
-//                     TMEM), operands staged by TMA (cp.async.bulk.tensor,
-//                     128-byte swizzle) in a ring of up to 8 stages.  Warp 0
-//                     issues the loads, warp 1 owns TMEM and issues the MMAs
-//                     (one thread), warps 2-5 drain TMEM with tcgen05.ld and
-//                     write Y.  A programmatic dependent of lora_t_kernel:
-//                     only the adapter step waits for it.
-// The GEMM is a persistent stream-K grid of at most one CTA per SM: the
-// (tile, K step) units are cut into equal ranges, so projections with few
-// weight tiles (N / 128 well below the 148 SMs) still fill the GPU.  A tile
-// cut by a range boundary is summed from fp32 partial tiles in CTA order by
-// the CTA holding its first K step, so results do not depend on timing.  The
-// host picks the grid from a cost model of K steps and epilogue costs.  The
-// last segment of a CTA's range writes its Y tile from the idle ring by TMA
-// store.
+// Kernels (three launches per slice of <= 448 token rows):
+//   lora_t_kernel      T = g s X A^T for every group (mma.sync, full K per
+//                      CTA, no cross-CTA sums), stored bf16 [M x groups*R64];
+//                      B padded to 64-value blocks where r % 64 != 0.
+//   lora_gemm_kernel   tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in
+//                      TMEM), operands staged by TMA (cp.async.bulk.tensor,
+//                      128-byte swizzle) in a ring of up to 8 stages.  Warp 0
+//                      issues the loads, warp 1 owns TMEM and issues the MMAs
+//                      (one thread), warps 2-5 drain TMEM with tcgen05.ld.
+//   lora_fixup_kernel  sums the fp32 partial tiles of every tile whose K sum
+//                      was split, in a fixed order, and writes its Y.
+// Work split of the GEMM over a persistent grid of at most one CTA per SM:
+// each CTA owns whole tiles (written as bf16 Y straight from TMEM) and an
+// equal share of the (tile, K step) units of the tiles left over (stream-K);
+// a segment of a left-over tile that a CTA does not hold whole is written as
+// an fp32 partial tile and summed by the fix-up kernel.  No CTA waits for
+// another, and the sums do not depend on timing.
 // Every mbarrier wait is bounded; a wait that runs out records
 // IDLM_DEV_TIMEOUT, and the CTA drains its copies and MMAs and frees its
 // tensor memory before it leaves.
 #include <algorithm>
-#include <atomic>
-#include <chrono>
 #include <cstdlib>
 #include <mutex>
 
@@ -67,66 +64,92 @@ constexpr uint32_t kAccCols = 256;         // one of two accumulators when m16 <
 constexpr uint32_t kWBytes = kTileN * kBK * 2;   // 16 KB
 constexpr uint32_t kStageY = 16 * kTileN * 2;    // Y staging: 16 tokens x 128 columns, bf16
 constexpr int kEpiBar = 1;                 // named barrier of the four epilogue warps
-constexpr int kMaxPSlots = 12;             // partial-tile pieces in flight (16 KB each)
-constexpr uint32_t kPiece = 16384;         // one piece: 32 tokens x 128 rows, fp32
 constexpr uint32_t kBarBytes = 512;
 constexpr int kYBoxRows = 16;              // token rows per TMA store of Y
+constexpr int kMaxGroups = 4;
+constexpr int kMaxRank = 128;
+constexpr int kPadW = 64;                  // adapter columns per K step
 
 struct Params {
   __nv_bfloat16* y;
-  float* part;              // [G][m16 / 4][128][4] fp32 partial tiles, one slot per CTA
-  unsigned long long* flag; // [G] = epoch once the CTA's partial tile is written
-  unsigned long long epoch; // distinct for every launch
-  unsigned long long wait_epoch;   // what a finaliser waits for (epoch, or a stale
-                                   // value under the failure-detection test switch)
-  unsigned long long flag_wait_ns; // limit of one finaliser wait
+  float4* part;             // [grid][2][m16 / 4][128] fp32 partial tiles (two slots per CTA)
   int32_t* status;
   int M, N, r;
   int m16;        // tokens rounded up to 16
   int n1, n2;     // MMA N of the two token blocks (n1 <= 256, n2 = m16 - n1)
-  int tiles, kb;  // weight-row tiles, K blocks
-  int S;          // K steps of a tile: kb K blocks, then the adapter step
-  long long U;    // tiles * S units of work, split evenly over the grid
+  int tiles, kb;  // weight-row tiles, K blocks of the base weight
+  int nad;        // adapter K steps (ceil(r / 64))
+  int S;          // K steps of a tile: kb, then nad
+  int sk_tiles;   // tiles [0, sk_tiles) are split by units; the rest are whole
+  int dp_per;     // whole tiles per CTA
+  long long U_sk; // sk_tiles * S
+  int ngroups;
+  int group_end[kMaxGroups];   // first tile after group g
+  int R64;        // adapter columns per group in T (r rounded up to 64)
   int stages;     // depth of the stage ring
   int nacc;       // accumulators in TMEM (2 when m16 <= 256)
   int yvec;       // Y rows allow 16-byte stores (N % 8 == 0, aligned base)
-  int pslots;     // 16 KB slots of the ring that stage partial tiles for the finaliser
-  int ytma;       // the last segment's Y tile goes out by TMA store from the ring
-  uint32_t ytile_off;   // ring offset of that [m16 x 128] bf16 tile
+  int ytma;       // the last whole tile goes out by TMA store from the ring
+  uint32_t ytile_off;     // ring offset of that [m16 x 128] bf16 tile
   uint32_t stage_bytes;   // one stage: the weight block, then the token rows
+  unsigned long long wait_ns;   // limit of one bounded wait
+  int test_stall;         // failure-detection test switch (see the entry point)
 };
 
-// Stream-K split of the work: the units (tile, k) in tile-major order are
-// cut into gridDim.x equal ranges, one per CTA.  A range is walked as
-// segments (its units within one tile).  Only the first segment of a range
-// can start inside a tile (k0 > 0): such a segment is a partial tile, stored
-// in fp32 in the CTA's workspace slot.  The CTA whose range holds (tile, 0)
-// and not the whole tile finalises it: it adds the partials of the next
-// CTAs (in CTA order) to its own accumulator and writes Y.  The partials
-// come from the beginnings of those CTAs' ranges, so they are ready long
-// before the finaliser, which reaches the tile at the end of its range.
+// A CTA's work, in order: the segments of its share of the split units, then
+// its whole tiles.  The producer, the MMA issuer and the epilogue walk the
+// same sequence.
 struct Seg {
   int tile, k0, k1;
+  bool first;     // the segment holding the start of the CTA's split share
+  bool last;      // the CTA's last segment (its ring is idle afterwards)
 };
-__device__ __forceinline__ long long range_begin(const Params& p, int c) {
-  return static_cast<long long>(c) * p.U / gridDim.x;
-}
-__device__ __forceinline__ Seg seg_at(const Params& p, long long pos, long long end) {
-  Seg s;
-  s.tile = static_cast<int>(pos / p.S);
-  s.k0 = static_cast<int>(pos - static_cast<long long>(s.tile) * p.S);
-  s.k1 = static_cast<int>(min(static_cast<long long>(p.S), end - static_cast<long long>(s.tile) * p.S));
-  return s;
+
+__device__ __forceinline__ long long sk_begin(const Params& p, int c) {
+  return static_cast<long long>(c) * p.U_sk / gridDim.x;
 }
 
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+struct SegWalk {
+  long long pos, end;
+  int dp_left, dp_next;
+  bool started;
+  __device__ SegWalk(const Params& p, int c) {
+    pos = sk_begin(p, c);
+    end = sk_begin(p, c + 1);
+    dp_left = p.dp_per;
+    dp_next = p.sk_tiles + c * p.dp_per;
+    started = false;
+  }
+  __device__ bool next(const Params& p, Seg& s) {
+    if (pos < end) {
+      s.tile = static_cast<int>(pos / p.S);
+      s.k0 = static_cast<int>(pos - static_cast<long long>(s.tile) * p.S);
+      s.k1 = static_cast<int>(min(static_cast<long long>(p.S), end - static_cast<long long>(s.tile) * p.S));
+      s.first = !started;
+      started = true;
+      pos = static_cast<long long>(s.tile) * p.S + s.k1;
+      s.last = pos >= end && dp_left == 0;
+      return true;
+    }
+    if (dp_left > 0) {
+      s.tile = dp_next++;
+      s.k0 = 0;
+      s.k1 = p.S;
+      s.first = false;
+      --dp_left;
+      s.last = dp_left == 0;
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ int group_of(const Params& p, int tile) {
+  int g = 0;
+  while (g + 1 < p.ngroups && tile >= p.group_end[g]) ++g;
+  return g;
 }
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
+
 // TMA store of a [rows x 128] bf16 box from shared memory (no swizzle).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -137,6 +160,24 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
 
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory");
+}
+
+// Bounded wait with a limit given per launch.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                             int32_t* status, unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (abort && *abort) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        if (abort) *abort = 1;
+        set_status(status, IDLM_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------- tcgen05 PTX
@@ -232,22 +273,16 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
 
 // ------------------------------------------------------------------ T = g s X A^T
 //
-// Grid: (row groups of 16 tokens) x (K slices of 512), then the CTAs that
-// pad B.  A CTA's 4 warps take 128 K values each of its slice and
-// accumulate the [16 x r] product X A^T with mma.sync (m16n8k16, bf16 in,
-// fp32 accumulate); the CTA adds its warps' sums in warp order and stores
-// the slice's fp32 partial.  The last CTA of a row group to finish (a
-// counter tagged with the launch's epoch, so the workspace needs no
-// clearing) adds the slices in slice order and stores T = g s (X A^T) in
-// bf16, [M x 64] with zeros past r and at rows with g = 0.  The padding CTAs
-// copy B [N x r] to B64 [N x 64] (zeros past r), so that both operands of
-// the LoRA step are plain 128-byte rows for TMA.  2 KB of shared memory, so
-// that these CTAs fit beside a GEMM CTA on one SM.
+// One CTA per block of 16 token rows x NJ*8 adapter columns (columns of all
+// groups, concatenated) with the whole K; its 8 warps take one eighth of K
+// each and accumulate with mma.sync (m16n8k16, bf16 in, fp32 accumulate),
+// then add their sums in warp order.  T = g s (X A^T) is stored in bf16 at
+// T64[m][group * R64 + j], zeros at gated-off rows and in the padding
+// columns j >= r.  Extra CTAs copy B to 64-value blocks (zeros past r)
+// where r % 64 != 0.
 constexpr int kTRows = 16;
-constexpr int kTThreads = 128;
+constexpr int kTThreads = 256;
 constexpr int kTWarps = kTThreads / 32;
-constexpr int kTSlice = 512;   // K values per CTA
-constexpr int kPadW = 64;      // padded LoRA rank
 
 __device__ __forceinline__ uint32_t ldg32(const __nv_bfloat16* p) {
   return __ldg(reinterpret_cast<const unsigned int*>(p));
@@ -255,127 +290,118 @@ __device__ __forceinline__ uint32_t ldg32(const __nv_bfloat16* p) {
 
 struct TParams {
   const __nv_bfloat16* x;
-  const __nv_bfloat16* a;
-  const __nv_bfloat16* b;
+  const __nv_bfloat16* a;       // [ngroups * r, K]
+  const __nv_bfloat16* b;       // [N, r]
   const uint8_t* gate;
   float scale;
-  int M, K, N, r;
-  int kslices;                  // ceil(K / kTSlice)
-  float* tpart;                 // [kslices][ceil(M / 16) * 16][kPadW] fp32
-  unsigned long long* tcount;   // [ceil(M / 16)]: epoch << 32 | slices done
-  unsigned long long epoch;
-  __nv_bfloat16* t64;
-  __nv_bfloat16* b64;
+  int M, K, N, r, ngroups, R64;
+  int nj;                       // 8-column MMA tiles per block (2 or 8)
+  int col_blocks;               // ceil(ngroups * r / (8 nj))
+  __nv_bfloat16* t64;           // [M, ngroups * R64]
+  __nv_bfloat16* b64;           // [N, R64]
 };
 
-__global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
-  __shared__ float red[kTWarps][kTRows][8];
-  __shared__ int last;
-  griddep_launch_dependents();
+template <int NJ>
+__device__ void t_block(const TParams& p, int m0, int j0) {
+  __shared__ float red[kTWarps][kTRows][8 * NJ];
+  __shared__ int any_gate;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rt = p.ngroups * p.r;
+  if (tid == 0) any_gate = 0;
+  __syncthreads();
+  if (tid < kTRows && m0 + tid < p.M && p.gate[m0 + tid]) atomicOr(&any_gate, 1);
+  __syncthreads();
+  const int g = lane >> 2, t4 = lane & 3;
+  float acc[NJ][4];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+  if (any_gate) {
+    const bool r0 = m0 + g < p.M, r1 = m0 + g + 8 < p.M;
+    const __nv_bfloat16* x0 = p.x + static_cast<size_t>(r0 ? m0 + g : 0) * p.K;
+    const __nv_bfloat16* x1 = p.x + static_cast<size_t>(r1 ? m0 + g + 8 : 0) * p.K;
+    const __nv_bfloat16* arow[NJ];
+    bool aval[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int col = j0 + j * 8 + g;
+      aval[j] = col < rt;
+      arow[j] = p.a + static_cast<size_t>(aval[j] ? col : 0) * p.K;
+    }
+    const int kper = (p.K + kTWarps * 16 - 1) / (kTWarps * 16) * 16;   // K per warp, 16s
+    const int kbeg = warp * kper, kend = min(p.K, kbeg + kper);
+#pragma unroll 2
+    for (int k16 = kbeg; k16 < kend; k16 += 16) {
+      const int k = k16 + 2 * t4;
+      const bool lo = k < p.K, hi = k + 8 < p.K;   // K % 8 == 0: pairs never straddle K
+      uint32_t af[4];
+      af[0] = (r0 && lo) ? ldg32(x0 + k) : 0u;
+      af[1] = (r1 && lo) ? ldg32(x1 + k) : 0u;
+      af[2] = (r0 && hi) ? ldg32(x0 + k + 8) : 0u;
+      af[3] = (r1 && hi) ? ldg32(x1 + k + 8) : 0u;
+      uint32_t bf[NJ][2];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        bf[j][0] = (aval[j] && lo) ? ldg32(arow[j] + k) : 0u;
+        bf[j][1] = (aval[j] && hi) ? ldg32(arow[j] + k + 8) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) mma_bf16_16816(acc[j], af, bf[j][0], bf[j][1]);
+    }
+  }
+  // the warps' sums, added in warp order
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    red[warp][g][8 * j + 2 * t4] = acc[j][0];
+    red[warp][g][8 * j + 2 * t4 + 1] = acc[j][1];
+    red[warp][g + 8][8 * j + 2 * t4] = acc[j][2];
+    red[warp][g + 8][8 * j + 2 * t4 + 1] = acc[j][3];
+  }
+  __syncthreads();
+  const size_t tstride = static_cast<size_t>(p.ngroups) * p.R64;
+  for (int e = tid; e < kTRows * NJ * 8; e += kTThreads) {
+    const int i = e / (NJ * 8), cl = e % (NJ * 8);
+    const int m = m0 + i, col = j0 + cl;
+    if (m >= p.M || col >= rt) continue;
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kTWarps; ++w) v += red[w][i][cl];
+    v = p.gate[m] ? v * p.scale : 0.f;
+    const int grp = col / p.r, jj = col % p.r;
+    p.t64[static_cast<size_t>(m) * tstride + grp * p.R64 + jj] = __float2bfloat16_rn(v);
+  }
+  // zeros in the padding columns of every group whose last real column this
+  // block holds
+  const int pad = p.R64 - p.r;
+  if (pad > 0) {
+    for (int e = tid; e < kTRows * p.ngroups * pad; e += kTThreads) {
+      const int i = e / (p.ngroups * pad), rem = e % (p.ngroups * pad);
+      const int grp = rem / pad, jj = p.r + rem % pad;
+      const int m = m0 + i;
+      const int last_col = grp * p.r + p.r - 1;
+      if (m < p.M && last_col >= j0 && last_col < j0 + NJ * 8)
+        p.t64[static_cast<size_t>(m) * tstride + grp * p.R64 + jj] = __float2bfloat16_rn(0.f);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
   const int groups = (p.M + kTRows - 1) / kTRows;
-  const int tblocks = groups * p.kslices;
+  const int tblocks = groups * p.col_blocks;
   if (static_cast<int>(blockIdx.x) >= tblocks) {
-    const int n = (blockIdx.x - tblocks) * kTThreads + tid;
+    // B -> B64: row n, 64-value blocks, zeros past r
+    const int n = (blockIdx.x - tblocks) * kTThreads + threadIdx.x;
     if (n < p.N) {
       const uint4* src = reinterpret_cast<const uint4*>(p.b + static_cast<size_t>(n) * p.r);
-      uint4* dst = reinterpret_cast<uint4*>(p.b64 + static_cast<size_t>(n) * kPadW);
-#pragma unroll
-      for (int q = 0; q < kPadW / 8; ++q)
-        dst[q] = q < p.r / 8 ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+      uint4* dst = reinterpret_cast<uint4*>(p.b64 + static_cast<size_t>(n) * p.R64);
+      for (int q = 0; q < p.R64 / 8; ++q) dst[q] = q < p.r / 8 ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
     }
     return;
   }
-  const int grp = blockIdx.x / p.kslices, ks = blockIdx.x % p.kslices;
-  const int m0 = grp * kTRows;
-  const int g = lane >> 2, t4 = lane & 3;
-  const int nt = p.r / 8;
-  float acc[8][4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-  const bool r0 = m0 + g < p.M, r1 = m0 + g + 8 < p.M;
-  const __nv_bfloat16* x0 = p.x + static_cast<size_t>(r0 ? m0 + g : 0) * p.K;
-  const __nv_bfloat16* x1 = p.x + static_cast<size_t>(r1 ? m0 + g + 8 : 0) * p.K;
-  const int kw = ks * kTSlice + warp * (kTSlice / kTWarps);
-#pragma unroll
-  for (int st = 0; st < kTSlice / kTWarps / 16; ++st) {
-    const int k = kw + st * 16 + 2 * t4;
-    const bool lo = k < p.K, hi = k + 8 < p.K;   // K % 8 == 0: pairs never straddle K
-    uint32_t af[4];
-    af[0] = (r0 && lo) ? ldg32(x0 + k) : 0u;
-    af[1] = (r1 && lo) ? ldg32(x1 + k) : 0u;
-    af[2] = (r0 && hi) ? ldg32(x0 + k + 8) : 0u;
-    af[3] = (r1 && hi) ? ldg32(x1 + k + 8) : 0u;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < nt) {
-        const __nv_bfloat16* ar = p.a + static_cast<size_t>(j * 8 + g) * p.K;
-        mma_bf16_16816(acc[j], af, lo ? ldg32(ar + k) : 0u, hi ? ldg32(ar + k + 8) : 0u);
-      }
-  }
-  // this slice's sum over its warps, in warp order
-  float* mine = p.tpart + (static_cast<size_t>(ks) * groups * kTRows + m0) * kPadW;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j >= nt) break;
-    red[warp][g][2 * t4] = acc[j][0];
-    red[warp][g][2 * t4 + 1] = acc[j][1];
-    red[warp][g + 8][2 * t4] = acc[j][2];
-    red[warp][g + 8][2 * t4 + 1] = acc[j][3];
-    __syncthreads();
-    {
-      const int i = tid / 8, c = tid % 8;
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kTWarps; ++w) v += red[w][i][c];
-      __stcg(mine + i * kPadW + j * 8 + c, v);
-    }
-    __syncthreads();
-  }
-  // the last slice of the row group to finish adds the slices in order
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned long long tag = (p.epoch & 0xffffffffull) << 32;
-    unsigned long long* cnt = p.tcount + grp;
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt), seen;
-    do {
-      seen = old;
-      const unsigned long long nv = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
-      old = atomicCAS(cnt, seen, nv);
-    } while (old != seen);
-    const unsigned long long now = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
-    last = (now & 0xffffffffull) == static_cast<unsigned long long>(p.kslices);
-    __threadfence();
-  }
-  __syncthreads();
-  if (!last) return;
-  // the r columns: slices added in slice order, 8 loads in flight at a time
-  for (int e = tid; e < kTRows * p.r; e += kTThreads) {
-    const int i = e / p.r, c = e % p.r, m = m0 + i;
-    if (m >= p.M) continue;
-    float v = 0.f;
-    if (p.gate[m]) {
-      const float* src = p.tpart + static_cast<size_t>(m) * kPadW + c;
-      const size_t stride = static_cast<size_t>(groups) * kTRows * kPadW;
-      for (int s0 = 0; s0 < p.kslices; s0 += 8) {
-        float u[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) u[q] = s0 + q < p.kslices ? __ldcg(src + (s0 + q) * stride) : 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (s0 + q < p.kslices) v += u[q];
-      }
-      v *= p.scale;
-    }
-    p.t64[static_cast<size_t>(m) * kPadW + c] = __float2bfloat16_rn(v);
-  }
-  for (int e = tid; e < kTRows * (kPadW - p.r); e += kTThreads) {
-    const int i = e / (kPadW - p.r), c = p.r + e % (kPadW - p.r), m = m0 + i;
-    if (m < p.M) p.t64[static_cast<size_t>(m) * kPadW + c] = __float2bfloat16_rn(0.f);
-  }
+  const int grp = blockIdx.x / p.col_blocks, cb = blockIdx.x % p.col_blocks;
+  if (p.nj == 8) t_block<8>(p, grp * kTRows, cb * 64);
+  else t_block<2>(p, grp * kTRows, cb * 16);
 }
 
 // ------------------------------------------------------------ the GEMM
@@ -392,19 +418,90 @@ inline size_t smem_bytes(int stages, uint32_t stage_bytes) {
   return 1024 + bar_offset(stages, stage_bytes) + kBarBytes;
 }
 
-// Spin (bounded by limit_ns) until *f == v with acquire semantics.
-__device__ bool wait_flag(const unsigned long long* f, unsigned long long v,
-                          unsigned long long limit_ns, int32_t* status) {
-  if (ld_acquire_u64(f) == v) return true;
-  const unsigned long long t0 = globaltimer();
-  while (ld_acquire_u64(f) != v) {
-    if (globaltimer() - t0 > limit_ns) {
-      set_status(status, IDLM_DEV_TIMEOUT);
-      return false;
+// Epilogue of a tile whose K sum this CTA holds whole: Y (bf16) for the
+// tile's 128 weight rows, through the 16-token staging buffer with 16-byte
+// stores of whole 256-byte rows.  Thread `row` owns weight row tile*128+row.
+__device__ __noinline__ void store_y_direct(const Params& p, uint32_t taddr, int n_base, int row,
+                                            int et, __nv_bfloat16* ystage) {
+  uint32_t ra[32];
+  for (int c0 = 0; c0 < p.m16; c0 += 32) {
+    tmem_ld32_async(taddr + c0, ra);
+    tmem_ld_wait(ra);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        ystage[j * kTileN + row] = __float2bfloat16_rn(__uint_as_float(ra[16 * h + j]));
+      epi_sync();
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int idx = it * 128 + et;
+        const int rr = idx >> 4, c8 = (idx & 15) * 8;
+        const int m = c0 + 16 * h + rr, n0 = n_base + c8;
+        if (m < p.M) {
+          const __nv_bfloat16* src = ystage + rr * kTileN + c8;
+          __nv_bfloat16* out = p.y + static_cast<size_t>(m) * p.N + n0;
+          if (p.yvec && n0 + 8 <= p.N) {
+            *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
+          } else {
+            for (int e = 0; e < 8; ++e)
+              if (n0 + e < p.N) out[e] = src[e];
+          }
+        }
+      }
+      epi_sync();
     }
-    __nanosleep(64);
   }
-  return true;
+}
+
+// The same for the CTA's last segment: the ring is idle, so the whole
+// [m16 x 128] bf16 tile is built there and leaves by TMA store.
+__device__ __noinline__ void store_y_tma(const Params& p, uint32_t taddr, int n_base, int row,
+                                         int et, __nv_bfloat16* ytile, const CUtensorMap* y_map) {
+  uint32_t ra[32];
+  for (int c0 = 0; c0 < p.m16; c0 += 32) {
+    tmem_ld32_async(taddr + c0, ra);
+    tmem_ld_wait(ra);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c0 + j < p.m16) ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(__uint_as_float(ra[j]));
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  epi_sync();
+  if (et == 0) {
+    for (int rb0 = 0; rb0 < p.m16; rb0 += kYBoxRows) tma_store_2d(y_map, ytile + rb0 * kTileN, n_base, rb0);
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  }
+  epi_sync();
+}
+
+// A partial tile (a segment of a split tile): fp32 [m16/4][128] float4 into
+// the CTA's slot, each store instruction a coalesced 2 KB row of float4s.
+// The next 32 columns are loaded from TMEM while this group's stores go out.
+__device__ __noinline__ void store_partial(const Params& p, uint32_t taddr, int row, float4* dst) {
+  uint32_t ra[32], rb[32];
+  tmem_ld32_async(taddr, ra);
+  for (int c0 = 0; c0 < p.m16; c0 += 64) {
+    tmem_ld_wait(ra);
+    const bool more = c0 + 32 < p.m16;
+    if (more) tmem_ld32_async(taddr + c0 + 32, rb);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (c0 + 4 * g < p.m16)
+        __stcg(dst + static_cast<size_t>(c0 / 4 + g) * kTileN + row,
+               make_float4(__uint_as_float(ra[4 * g]), __uint_as_float(ra[4 * g + 1]),
+                           __uint_as_float(ra[4 * g + 2]), __uint_as_float(ra[4 * g + 3])));
+    if (!more) break;
+    tmem_ld_wait(rb);
+    if (c0 + 64 < p.m16) tmem_ld32_async(taddr + c0 + 64, ra);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (c0 + 32 + 4 * g < p.m16)
+        __stcg(dst + static_cast<size_t>((c0 + 32) / 4 + g) * kTileN + row,
+               make_float4(__uint_as_float(rb[4 * g]), __uint_as_float(rb[4 * g + 1]),
+                           __uint_as_float(rb[4 * g + 2]), __uint_as_float(rb[4 * g + 3])));
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -421,14 +518,12 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
   uint64_t* empty = bars + kMaxStages;          // [stages] MMA -> TMA
   uint64_t* tmem_full = bars + 2 * kMaxStages;  // [2] MMA -> epilogue
   uint64_t* tmem_empty = tmem_full + 2;         // [2] epilogue -> MMA
-  uint64_t* drain = tmem_empty + 2;             // MMA issuer, after an abort
-  uint64_t* pbar = drain + 1;                   // [kMaxPSlots] partial pieces -> finaliser
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(pbar + kMaxPSlots);
+  uint64_t* drain = tmem_empty + 2;             // MMA issuer: every MMA finished
+  uint64_t* never = drain + 1;                  // nothing arrives here (test switch)
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base + 1);
-  volatile int* epi_fail = abort_flag + 1;      // set by an epilogue warp, read after epi_sync
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long r_begin = range_begin(p, blockIdx.x), r_end = range_begin(p, blockIdx.x + 1);
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -439,9 +534,8 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
       mbar_init(&tmem_empty[a], 4);   // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
-    for (int i = 0; i < kMaxPSlots; ++i) mbar_init(&pbar[i], 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
-    *epi_fail = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -452,6 +546,8 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base;
+  // the fix-up kernel may be scheduled; it waits for this grid to finish
+  griddep_launch_dependents();
 
   // The producer and MMA warps run their loops with all 32 lanes (the waits
   // are warp-uniform); lane 0 issues the copies and the MMAs.
@@ -465,35 +561,35 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
     const uint32_t tx = kWBytes + static_cast<uint32_t>(p.m16) * 128;
     int issued = 0;
     bool ok = true;
-    bool t_ready = false;
-    for (long long pos = r_begin; ok && pos < r_end;) {
-      const Seg sg = seg_at(p, pos, r_end);
+    // X, B and T come from the kernels before this one in the stream (this
+    // grid may have been launched as a programmatic dependent)
+    griddep_wait();
+    SegWalk wk(p, blockIdx.x);
+    Seg sg;
+    while (ok && wk.next(p, sg)) {
+      const int grp = group_of(p, sg.tile);
       for (int k = sg.k0; k < sg.k1; ++k, ++issued) {
         const int s = issued % p.stages;
         const uint32_t ph = (issued / p.stages) & 1;
-        if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status)) {
+        if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, p.wait_ns)) {
           ok = false;
           break;
         }
-        const bool lora_step = k == p.kb;   // B and T, written by lora_t_kernel
-        if (lora_step && !t_ready) {
-          griddep_wait();
-          t_ready = true;
-        }
+        const bool lora_step = k >= p.kb;   // B and T, written by lora_t_kernel
         if (lane == 0) {
           uint8_t* st = base + size_t(s) * p.stage_bytes;
           const CUtensorMap* am = lora_step ? &b_map : &w_map;
           const CUtensorMap* bm1 = lora_step ? &t_map1 : &x_map1;
           const CUtensorMap* bm2 = lora_step ? &t_map2 : &x_map2;
-          const int kx = lora_step ? 0 : k * kBK;
+          const int ka = lora_step ? (k - p.kb) * kBK : k * kBK;
+          const int kt = lora_step ? grp * p.R64 + (k - p.kb) * kBK : k * kBK;
           mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_2d(st, am, &full[s], kx, sg.tile * kTileN);
-          tma_load_2d(st + kWBytes, bm1, &full[s], kx, 0);
-          if (p.n2) tma_load_2d(st + kWBytes + p.n1 * 128, bm2, &full[s], kx, p.n1);
+          tma_load_2d(st, am, &full[s], ka, sg.tile * kTileN);
+          tma_load_2d(st + kWBytes, bm1, &full[s], kt, 0);
+          if (p.n2) tma_load_2d(st + kWBytes + p.n1 * 128, bm2, &full[s], kt, p.n1);
         }
         __syncwarp();
       }
-      pos = static_cast<long long>(sg.tile) * p.S + sg.k1;
     }
     // every copy into the ring lands before the CTA may leave
     for (int i = max(0, issued - p.stages); i < issued; ++i)
@@ -502,22 +598,23 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
     // --------------------------------------------------------- MMA issuer
     const uint32_t idesc1 = make_idesc(kTileN, p.n1);
     const uint32_t idesc2 = make_idesc(kTileN, p.n2 ? p.n2 : 16);
-    const int ksub_lora = (p.r + 15) / 16;
     int consumed = 0, t_iter = 0;
     bool ok = true;
-    for (long long pos = r_begin; ok && pos < r_end; ++t_iter) {
-      const Seg sg = seg_at(p, pos, r_end);
-      pos = static_cast<long long>(sg.tile) * p.S + sg.k1;
+    if (p.test_stall && !wait_bounded(never, 0, abort_flag, p.status, p.wait_ns)) ok = false;
+    SegWalk wk(p, blockIdx.x);
+    Seg sg;
+    while (ok && wk.next(p, sg)) {
       const int a = t_iter % p.nacc;
       const uint32_t use = t_iter / p.nacc;
+      ++t_iter;
       // the epilogue has drained this accumulator's previous segment
-      if (!mbar_wait_bounded(&tmem_empty[a], (use & 1) ^ 1, abort_flag, p.status)) break;
+      if (!wait_bounded(&tmem_empty[a], (use & 1) ^ 1, abort_flag, p.status, p.wait_ns)) break;
       tc_fence_after();
       const uint32_t d = tmem + a * kAccCols;
       for (int k = sg.k0; k < sg.k1; ++k, ++consumed) {
         const int s = consumed % p.stages;
         const uint32_t ph = (consumed / p.stages) & 1;
-        if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.status)) {
+        if (!wait_bounded(&full[s], ph, abort_flag, p.status, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -527,7 +624,7 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
           const uint64_t a_desc = make_sdesc(sa);
           const uint64_t b1_desc = make_sdesc(sa + kWBytes);
           const uint64_t b2_desc = make_sdesc(sa + kWBytes + p.n1 * 128);
-          const int nsub = k < p.kb ? kBK / 16 : ksub_lora;
+          const int nsub = k < p.kb ? kBK / 16 : (min(kBK, p.r - (k - p.kb) * kBK) + 15) / 16;
           for (int j = 0; j < nsub; ++j) {
             // advance 16 values (32 bytes) along K inside the swizzled rows
             const uint64_t off = static_cast<uint64_t>(j * 2);
@@ -543,11 +640,9 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
       __syncwarp();
     }
     // no MMA may still run when the tensor memory is freed
-    if (*abort_flag) {
-      if (lane == 0) mma_commit(drain);
-      __syncwarp();
-      mbar_wait_bounded(drain, 0, nullptr, p.status);
-    }
+    if (lane == 0) mma_commit(drain);
+    __syncwarp();
+    mbar_wait_bounded(drain, 0, nullptr, p.status);
   } else {
     // ---------------------------------------------------------- epilogue
     // Thread `row` (0..127) owns weight row tile * 128 + row: TMEM lane row.
@@ -557,164 +652,27 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
     const int row = q * 32 + lane;
     const int et = tid - 64;   // 0..127
     const int nq = p.m16 / 4;  // float4 groups of a partial tile row
-    const float4* part4 = reinterpret_cast<const float4*>(p.part);
+    __nv_bfloat16* ytile = reinterpret_cast<__nv_bfloat16*>(base + p.ytile_off);
     int t_iter = 0;
-    for (long long pos = r_begin; pos < r_end; ++t_iter) {
-      const Seg sg = seg_at(p, pos, r_end);
-      pos = static_cast<long long>(sg.tile) * p.S + sg.k1;
+    SegWalk wk(p, blockIdx.x);
+    Seg sg;
+    while (wk.next(p, sg)) {
       const int a = t_iter % p.nacc;
       const uint32_t use = t_iter / p.nacc;
-      if (!mbar_wait_bounded(&tmem_full[a], use & 1, nullptr, p.status)) {
-        *epi_fail = 1;
-        *abort_flag = 1;
-      }
+      ++t_iter;
+      wait_bounded(&tmem_full[a], use & 1, abort_flag, p.status, p.wait_ns);
       epi_sync();
-      if (*epi_fail) break;
+      if (*abort_flag) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * kAccCols;
-      uint32_t ra[32];
-      if (sg.k0 > 0) {
-        // a partial tile: into this CTA's workspace slot, then the flag
-        float4* dst = reinterpret_cast<float4*>(p.part) + static_cast<size_t>(blockIdx.x) * nq * kTileN;
-        for (int c0 = 0; c0 < p.m16; c0 += 32) {
-          tmem_ld32_async(taddr + c0, ra);
-          tmem_ld_wait(ra);
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (c0 + 4 * g < p.m16)
-              __stcg(dst + static_cast<size_t>(c0 / 4 + g) * kTileN + row,
-                     make_float4(__uint_as_float(ra[4 * g]), __uint_as_float(ra[4 * g + 1]),
-                                 __uint_as_float(ra[4 * g + 2]), __uint_as_float(ra[4 * g + 3])));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tmem_empty[a]);
-        __threadfence();
-        epi_sync();
-        if (et == 0) st_release_u64(&p.flag[blockIdx.x], p.epoch);
-        continue;
-      }
-      // A whole tile, or the head of a tile whose other segments are the
-      // partials of the next CTAs.  Those arrive in 16 KB pieces (32 tokens
-      // of one partial) by bulk copy into the ring, which is idle now: the
-      // head is the last segment of this CTA's range.
-      int c_lo = blockIdx.x + 1, c_hi = c_lo;
-      if (sg.k1 < p.S) {
-        const long long tile_end = static_cast<long long>(sg.tile + 1) * p.S;
-        while (c_hi < static_cast<int>(gridDim.x) && range_begin(p, c_hi) < tile_end) ++c_hi;
-        if (et == 0) {
-          for (int c = c_lo; c < c_hi; ++c)
-            if (!wait_flag(&p.flag[c], p.wait_epoch, p.flag_wait_ns, p.status)) {
-              *epi_fail = 1;
-              *abort_flag = 1;
-              break;
-            }
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-        }
-        epi_sync();
-        if (*epi_fail) break;
-      }
-      const int ncon = c_hi - c_lo;
-      const int npieces = ((p.m16 + 31) / 32) * ncon;
-      int issued = 0;
-      // issue pieces [issued, upto) into their slots
-      auto issue = [&](int upto) {
-        for (; issued < upto && issued < npieces; ++issued) {
-          const int ch = issued / ncon, c = c_lo + issued % ncon, slot = issued % p.pslots;
-          const uint32_t bytes = static_cast<uint32_t>(min(32, p.m16 - ch * 32) / 4) * kTileN * 16;
-          mbar_arrive_expect_tx(&pbar[slot], bytes);
-          bulk_g2s(base + size_t(slot) * kPiece,
-                   part4 + (static_cast<size_t>(c) * nq + ch * 8) * kTileN, bytes, &pbar[slot]);
-        }
-      };
-      if (et == 0) issue(p.pslots);
-      const int n_base = sg.tile * kTileN;
-      // The last segment of the range has the ring to itself: its Y tile is
-      // built there whole and leaves by TMA store (no per-chunk barriers).
-      const bool tma_y = p.ytma && pos == r_end;
-      __nv_bfloat16* ytile = reinterpret_cast<__nv_bfloat16*>(base + p.ytile_off);
-      // The common case (a whole tile at the end of the range) gets a loop of
-      // its own: small enough to stay in the instruction cache.
-      for (int c0 = 0; tma_y && ncon == 0 && c0 < p.m16; c0 += 32) {
-        tmem_ld32_async(taddr + c0, ra);
-        tmem_ld_wait(ra);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < p.m16) ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(__uint_as_float(ra[j]));
-      }
-      for (int c0 = 0, ch = 0; !(tma_y && ncon == 0) && c0 < p.m16; c0 += 32, ++ch) {
-        tmem_ld32_async(taddr + c0, ra);
-        tmem_ld_wait(ra);
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ra[j]);
-        for (int ci = 0; ci < ncon; ++ci) {   // partials in CTA order
-          const int pidx = ch * ncon + ci, slot = pidx % p.pslots;
-          mbar_wait_bounded(&pbar[slot], (pidx / p.pslots) & 1, nullptr, p.status);
-          const float4* sp = reinterpret_cast<const float4*>(base + size_t(slot) * kPiece);
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (c0 + 4 * g < p.m16) {
-              const float4 u = sp[g * kTileN + row];
-              v[4 * g] += u.x;
-              v[4 * g + 1] += u.y;
-              v[4 * g + 2] += u.z;
-              v[4 * g + 3] += u.w;
-            }
-          // more partials than slots: refill after every full round of slots
-          if ((pidx + 1) % p.pslots == 0 && ci + 1 < ncon) {
-            epi_sync();
-            if (et == 0) issue(pidx + 1 + p.pslots);
-          }
-        }
-        if (tma_y) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c0 + j < p.m16) ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(v[j]);
-          if (ncon) {   // every thread is done with this chunk's pieces: refill their slots
-            epi_sync();
-            if (et == 0) issue((ch + 1) * ncon + p.pslots);
-          }
-          continue;
-        }
-        // Y[c0 .. c0 + 31][n_base .. n_base + 127] through shared memory, 16
-        // tokens at a time, so that the global stores are 16-byte pieces of
-        // whole 256-byte rows
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) ystage[j * kTileN + row] = __float2bfloat16_rn(v[16 * h + j]);
-          epi_sync();
-          // every thread is done with this chunk's pieces: refill their slots
-          if (h == 0 && et == 0 && ncon) issue((ch + 1) * ncon + p.pslots);
-#pragma unroll
-          for (int it = 0; it < 2; ++it) {
-            const int idx = it * 128 + et;
-            const int rr = idx >> 4, c8 = (idx & 15) * 8;
-            const int m = c0 + 16 * h + rr, n0 = n_base + c8;
-            if (m < p.M) {
-              const __nv_bfloat16* src = ystage + rr * kTileN + c8;
-              __nv_bfloat16* out = p.y + static_cast<size_t>(m) * p.N + n0;
-              if (p.yvec && n0 + 8 <= p.N) {
-                *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
-              } else {
-                for (int e = 0; e < 8; ++e)
-                  if (n0 + e < p.N) out[e] = src[e];
-              }
-            }
-          }
-          epi_sync();
-        }
-      }
-      if (tma_y) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        epi_sync();
-        if (et == 0) {
-          for (int rb0 = 0; rb0 < p.m16; rb0 += kYBoxRows)
-            tma_store_2d(&y_map, ytile + rb0 * kTileN, n_base, rb0);
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        }
+      if (sg.k0 == 0 && sg.k1 == p.S) {
+        const int n_base = sg.tile * kTileN;
+        if (p.ytma && sg.last) store_y_tma(p, taddr, n_base, row, et, ytile, &y_map);
+        else store_y_direct(p, taddr, n_base, row, et, ystage);
+      } else {
+        const int slot = sg.first ? 0 : 1;
+        store_partial(p, taddr, row,
+                      p.part + (static_cast<size_t>(blockIdx.x) * 2 + slot) * nq * kTileN);
       }
       tc_fence_before();
       __syncwarp();
@@ -730,6 +688,65 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
   }
 }
 
+// ------------------------------------------------------------ fix-up
+//
+// One CTA per (split tile, 32 tokens): the fp32 partials of the CTAs whose
+// split shares cut the tile are added in CTA order (each CTA's segment of a
+// tile is a contiguous K range, so this is the order of K), then Y.
+struct FParams {
+  const float4* part;
+  __nv_bfloat16* y;
+  long long U_sk;
+  int S, G, M, N, m16, sk_tiles;
+};
+
+__device__ __forceinline__ long long fx_begin(const FParams& f, int c) {
+  return static_cast<long long>(c) * f.U_sk / f.G;
+}
+
+__global__ void __launch_bounds__(128) lora_fixup_kernel(const FParams f) {
+  griddep_wait();
+  const int chunks = (f.m16 + 31) / 32;
+  const int t = blockIdx.x / chunks, ch = blockIdx.x % chunks;
+  if (t >= f.sk_tiles) return;
+  const long long u0 = static_cast<long long>(t) * f.S, u1 = u0 + f.S;
+  // CTAs whose shares meet [u0, u1): the owner of unit x is the largest c
+  // with begin(c) <= x
+  const int c_first = static_cast<int>(((u0 + 1) * f.G - 1) / f.U_sk);
+  const int c_last = static_cast<int>((u1 * f.G - 1) / f.U_sk);
+  if (c_first == c_last && fx_begin(f, c_first) <= u0 && fx_begin(f, c_first + 1) >= u1)
+    return;   // one CTA held the tile whole and wrote its Y
+  const int row = threadIdx.x;
+  const int nq = f.m16 / 4;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = 0.f;
+  for (int c = c_first; c <= c_last; ++c) {
+    const long long b = fx_begin(f, c), e = fx_begin(f, c + 1);
+    if (b >= e) continue;
+    const int slot = (c == c_first && b < u0) ? 1 : 0;
+    const float4* src = f.part + (static_cast<size_t>(c) * 2 + slot) * nq * kTileN;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const int col4 = ch * 8 + g;
+      if (col4 < nq) {
+        const float4 u = __ldcg(src + static_cast<size_t>(col4) * kTileN + row);
+        v[4 * g] += u.x;
+        v[4 * g + 1] += u.y;
+        v[4 * g + 2] += u.z;
+        v[4 * g + 3] += u.w;
+      }
+    }
+  }
+  const int n = t * kTileN + row;
+  if (n >= f.N) return;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int m = ch * 32 + j;
+    if (m < f.M) f.y[static_cast<size_t>(m) * f.N + n] = __float2bfloat16_rn(v[j]);
+  }
+}
+
 }  // namespace lora
 }  // namespace idlm
 
@@ -737,8 +754,8 @@ using namespace idlm;
 
 namespace {
 
-// CTAs of the stream-K grid at most: the SMs of the current device (one CTA
-// per SM), or 256 where no device can be queried.
+// CTAs of the GEMM grid at most: the SMs of the current device (one CTA per
+// SM), or 256 where no device can be queried.
 int max_grid() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -749,97 +766,112 @@ int max_grid() {
   return std::min(n, 256);
 }
 
+int r64_of(int r) { return (r + lora::kPadW - 1) / lora::kPadW * lora::kPadW; }
+
 struct WsLayout {
-  size_t t64, b64, tpart, tcount, flag, part, total;
+  size_t t64, b64, part, total;
 };
-WsLayout ws_layout(int M, int K, int N) {
+WsLayout ws_layout(int M, int N, int r, int ngroups) {
   const int Ms = std::min(M, lora::kMaxTokens);
   const size_t m16 = (Ms + 15) / 16 * 16;
-  const size_t ks = (K + lora::kTSlice - 1) / lora::kTSlice;
   const size_t G = max_grid();
+  const size_t R64 = r64_of(r);
   WsLayout l;
   l.t64 = 0;
-  l.b64 = align_up(static_cast<size_t>(Ms) * lora::kPadW * 2, 256);
-  l.tpart = l.b64 + align_up(static_cast<size_t>(N) * lora::kPadW * 2, 256);
-  l.tcount = l.tpart + align_up(ks * m16 * lora::kPadW * sizeof(float), 256);
-  l.flag = l.tcount + align_up(m16 / 16 * sizeof(unsigned long long), 256);
-  l.part = l.flag + align_up(G * sizeof(unsigned long long), 256);
-  l.total = l.part + G * lora::kTileN * m16 * sizeof(float);
+  l.b64 = align_up(static_cast<size_t>(Ms) * ngroups * R64 * 2, 256);
+  l.part = l.b64 + align_up(static_cast<size_t>(N) * R64 * 2, 256);
+  l.total = l.part + G * 2 * lora::kTileN * m16 * sizeof(float);
   return l;
 }
 
 struct LoraPlan {
-  int m16, n1, n2, tiles, kb, S, stages, nacc, grid;
-  long long U;
+  int m16, n1, n2, tiles, kb, nad, S, nacc, grid, sk_tiles, dp_per;
+  long long U_sk;
   uint32_t stage_bytes;
-  size_t smem;
 };
 
-// Grid size of the stream-K split by a cost model in microseconds, fitted to
-// B300 timings of this kernel at 448 tokens: a K step of the 128 x 448 tile
-// takes about 0.63 us (the MMAs near the measured bf16 peak rate and the TMA
-// ingest of its 73 KB of operands); an epilogue that writes a Y tile about
-// 10 us, one that writes a 229 KB fp32 partial tile about 5 us, and a
-// finaliser about 10 us more per partial it adds.  All but a quarter of the
-// step and all of the epilogue scale with the tokens.  Every CTA's range
-// holds at least one unit, and the grid never exceeds the SMs, so that all
-// CTAs are resident at once (a finaliser waits for CTAs after it).
-LoraPlan plan_for(int M, int K, int N, int grid_cap) {
+// Grid of the GEMM by a cost model in microseconds (B300, 448 tokens): a K
+// step of the 128 x 448 tile about 0.65 us (the MMAs near the measured bf16
+// rate); an fp32 partial tile about 2 us to write, a whole tile's Y about
+// 3 us, and the fix-up kernel about 3 us plus its share of the partial
+// bytes.  A quarter of a K step and the epilogues scale with the tokens.  A
+// grid of G CTAs holds floor(tiles / G) whole tiles each and splits the
+// other tiles' units evenly.
+LoraPlan plan_for(int M, int K, int N, int r, int grid_cap) {
   LoraPlan pl;
   pl.m16 = (M + 15) / 16 * 16;
   pl.n1 = std::min(256, pl.m16);
   pl.n2 = pl.m16 - pl.n1;
   pl.tiles = (N + lora::kTileN - 1) / lora::kTileN;
   pl.kb = (K + lora::kBK - 1) / lora::kBK;
-  pl.S = pl.kb + 1;
-  pl.U = static_cast<long long>(pl.tiles) * pl.S;
+  pl.nad = (r + lora::kPadW - 1) / lora::kPadW;
+  pl.S = pl.kb + pl.nad;
   pl.stage_bytes = lora::kWBytes + static_cast<uint32_t>(pl.m16) * 128;   // 2 KB multiple
   pl.nacc = pl.m16 <= static_cast<int>(lora::kAccCols) ? 2 : 1;
   const double f = pl.m16 / 448.0;
-  const double step = 0.63 * (0.25 + 0.75 * f);
-  double best = 1e300;
-  pl.grid = 1;
-  const long long gmax = std::min<long long>(grid_cap, pl.U);
+  const double step = 0.65 * (0.25 + 0.75 * f);
+  const long long units = static_cast<long long>(pl.tiles) * pl.S;
+  const long long gmax = std::min<long long>(grid_cap, units);
+  auto split = [&](long long G, int& dp, int& skt, long long& usk) {
+    dp = static_cast<int>(pl.tiles / G);
+    skt = pl.tiles - dp * static_cast<int>(G);
+    usk = static_cast<long long>(skt) * pl.S;
+  };
   const char* force = std::getenv("IDLM_LORA_GRID");
   if (force && std::atoll(force) > 0) {   // a fixed grid (the tests cover several)
     pl.grid = static_cast<int>(std::min<long long>(gmax, std::atoll(force)));
+    split(pl.grid, pl.dp_per, pl.sk_tiles, pl.U_sk);
     return pl;
   }
+  double best = 1e300;
+  pl.grid = 1;
   for (long long G = 1; G <= gmax; ++G) {
-    const long long per = (pl.U + G - 1) / G, minseg = pl.U / G;
-    const bool split = pl.U % G != 0 || (pl.U / G) % pl.S != 0;
-    const long long contrib = split ? (pl.S + minseg - 1) / minseg : 0;
-    const double ytiles = std::max(1.0, static_cast<double>(per) / pl.S);
-    const double t = per * step + (split ? (5.0 + 10.0 * contrib) * f : 0.0) + 10.0 * f * ytiles;
+    int dp, skt;
+    long long usk;
+    split(G, dp, skt, usk);
+    const long long sk_per = (usk + G - 1) / G;
+    const bool cut = usk > 0 && (usk % G != 0 || (usk / G) % pl.S != 0);
+    const double part_mb =
+        cut ? static_cast<double>(std::min<long long>(2 * G, skt + G)) * pl.m16 * lora::kTileN * 4 / 1e6
+            : 0.0;
+    const double t = (dp * pl.S + sk_per) * step + (dp ? 3.0 * f : 0.0) +
+                     (cut ? 2.0 * f + 3.0 + part_mb / (0.1 * G) : (usk ? 3.0 * f : 0.0));
     if (t < best * 0.98) {
       best = t;
       pl.grid = static_cast<int>(G);
     }
   }
+  split(pl.grid, pl.dp_per, pl.sk_tiles, pl.U_sk);
   return pl;
 }
 
-}  // namespace
-
-extern "C" size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r) {
-  if (M <= 0 || K <= 0 || N <= 0 || r <= 0) return 0;
-  return ws_layout(M, K, N).total;
-}
-
-extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void* lora_a,
-                                       const void* lora_b, const uint8_t* row_gate,
-                                       float lora_scale, int M, int K, int N, int r, void* y,
-                                       void* workspace, size_t workspace_bytes, int32_t* status,
-                                       void* stream_) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (!x || !w || !lora_a || !lora_b || !row_gate || !y || !status) return IDLM_ERR_INVALID_ARG;
-  if (M <= 0 || K <= 0 || N <= 0 || r <= 0) return IDLM_ERR_INVALID_ARG;
-  if (K % 8 || r % 8 || r > 64) return IDLM_ERR_UNSUPPORTED;
+idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, const void* lora_b,
+                            const uint8_t* row_gate, float lora_scale, int M, int K, int N, int r,
+                            int ngroups, const int* group_rows, void* y, void* workspace,
+                            size_t workspace_bytes, int32_t* status, cudaStream_t stream) {
+  if (!x || !w || !y || !status) return IDLM_ERR_INVALID_ARG;
+  if (r > 0 && (!lora_a || !lora_b || !row_gate)) return IDLM_ERR_INVALID_ARG;
+  if (M <= 0 || K <= 0 || N <= 0 || r < 0 || ngroups < 1) return IDLM_ERR_INVALID_ARG;
+  if (ngroups > lora::kMaxGroups || K % 8 || r % 8 || r > lora::kMaxRank) return IDLM_ERR_UNSUPPORTED;
+  int gend_rows[lora::kMaxGroups] = {0, 0, 0, 0};
+  if (ngroups > 1) {
+    if (!group_rows) return IDLM_ERR_INVALID_ARG;
+    int acc = 0;
+    for (int g = 0; g < ngroups; ++g) {
+      if (group_rows[g] <= 0) return IDLM_ERR_INVALID_ARG;
+      if (group_rows[g] % lora::kTileN && g + 1 < ngroups) return IDLM_ERR_UNSUPPORTED;
+      acc += group_rows[g];
+      gend_rows[g] = acc;
+    }
+    if (acc != N) return IDLM_ERR_INVALID_ARG;
+  } else {
+    gend_rows[0] = N;
+  }
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
        reinterpret_cast<uintptr_t>(lora_a) | reinterpret_cast<uintptr_t>(lora_b)) & 15)
     return IDLM_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < idlm_gated_lora_workspace_size(M, K, N, r) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255))
+  const WsLayout wl = ws_layout(M, N, r, ngroups);
+  if (!workspace || workspace_bytes < wl.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return IDLM_ERR_WORKSPACE;
   DeviceInfo dev;
   if (!current_device_info(&dev)) return IDLM_ERR_CUDA;
@@ -853,29 +885,30 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
       if (cudaFuncSetAttribute(lora::lora_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dev.max_smem_optin) != cudaSuccess)
         return IDLM_ERR_CUDA;
-      // the adapter kernel's CTAs run beside GEMM CTAs: keep the SM's
-      // shared-memory carveout at its maximum for both
-      if (cudaFuncSetAttribute(lora::lora_t_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-        return IDLM_ERR_CUDA;
       done[dev.device] = ctx;
     }
   }
-  // launches get distinct epochs, so the flags never need clearing
-  static std::atomic<unsigned long long> epoch_counter{
-      0x9e3779b97f4a7c15ull ^
-      static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};
-  const WsLayout wl = ws_layout(M, K, N);
+  // Failure-detection test switch: with IDLM_TEST_STALL=1 the MMA issuer of
+  // every GEMM CTA first waits (20 ms) on an mbarrier that nothing arrives
+  // on, so the call ends with TIMEOUT in the status word.
+  const char* stall = std::getenv("IDLM_TEST_STALL");
+  const bool test_stall = stall && stall[0] == '1';
+  const int R64 = r64_of(r);
+  const bool pad_b = r > 0 && (r % lora::kPadW) != 0;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(wsb + wl.t64);
-  __nv_bfloat16* b64 = reinterpret_cast<__nv_bfloat16*>(wsb + wl.b64);
+  __nv_bfloat16* b64 = pad_b ? reinterpret_cast<__nv_bfloat16*>(wsb + wl.b64)
+                             : const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(lora_b));
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
   const int grid_cap = std::min(dev.sm_count, max_grid());
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
   // token rows in slices of at most 448 (the tensor-memory columns and the ring)
   for (int m0 = 0; m0 < M; m0 += lora::kMaxTokens) {
     const int Ms = std::min(lora::kMaxTokens, M - m0);
-    const LoraPlan pl = plan_for(Ms, K, N, grid_cap);
+    const LoraPlan pl = plan_for(Ms, K, N, r, grid_cap);
     const int stages = std::min<int>(
         lora::kMaxStages,
         static_cast<int>((dev.max_smem_optin - 1024 - lora::kBarBytes - lora::kStageY) /
@@ -884,6 +917,7 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
     // at least 120 KB, so that one CTA holds an SM (and its tensor memory)
     const size_t smem = std::max<size_t>(lora::smem_bytes(stages, pl.stage_bytes), 120 * 1024);
     const __nv_bfloat16* xs = xb + static_cast<size_t>(m0) * K;
+    const int tcols = ngroups * R64;
     CUtensorMap wm, xm1, xm2, bm, tm1, tm2;
     const uint64_t wdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
     const uint64_t wstr[1] = {static_cast<uint64_t>(K) * 2};
@@ -891,18 +925,24 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
     const uint64_t xdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(Ms)};
     const uint32_t xbox1[2] = {lora::kBK, static_cast<uint32_t>(pl.n1)};
     const uint32_t xbox2[2] = {lora::kBK, static_cast<uint32_t>(pl.n2 ? pl.n2 : 16)};
-    const uint64_t bdims[2] = {static_cast<uint64_t>(lora::kPadW), static_cast<uint64_t>(N)};
-    const uint64_t rstr[1] = {static_cast<uint64_t>(lora::kPadW) * 2};
-    const uint64_t tdims[2] = {static_cast<uint64_t>(lora::kPadW), static_cast<uint64_t>(Ms)};
+    const uint64_t bdims[2] = {static_cast<uint64_t>(R64), static_cast<uint64_t>(N)};
+    const uint64_t bstr[1] = {static_cast<uint64_t>(R64) * 2};
+    const uint64_t tdims[2] = {static_cast<uint64_t>(tcols), static_cast<uint64_t>(Ms)};
+    const uint64_t tstr[1] = {static_cast<uint64_t>(tcols) * 2};
     if (!encode_bf16_map(&wm, const_cast<void*>(w), 2, wdims, wstr, wbox) ||
         !encode_bf16_map(&xm1, const_cast<__nv_bfloat16*>(xs), 2, xdims, wstr, xbox1) ||
-        !encode_bf16_map(&xm2, const_cast<__nv_bfloat16*>(xs), 2, xdims, wstr, xbox2) ||
-        !encode_bf16_map(&bm, b64, 2, bdims, rstr, wbox) ||
-        !encode_bf16_map(&tm1, t, 2, tdims, rstr, xbox1) ||
-        !encode_bf16_map(&tm2, t, 2, tdims, rstr, xbox2))
+        !encode_bf16_map(&xm2, const_cast<__nv_bfloat16*>(xs), 2, xdims, wstr, xbox2))
       return IDLM_ERR_CUDA;
+    if (r == 0) {   // no adapter steps: these maps are never used
+      bm = wm;
+      tm1 = xm1;
+      tm2 = xm2;
+    } else if (!encode_bf16_map(&bm, b64, 2, bdims, bstr, wbox) ||
+               !encode_bf16_map(&tm1, t, 2, tdims, tstr, xbox1) ||
+               !encode_bf16_map(&tm2, t, 2, tdims, tstr, xbox2)) {
+      return IDLM_ERR_CUDA;
+    }
 
-    const unsigned long long epoch = ++epoch_counter;
     lora::TParams tp;
     tp.x = xs;
     tp.a = static_cast<const __nv_bfloat16*>(lora_a);
@@ -913,29 +953,23 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
     tp.K = K;
     tp.N = N;
     tp.r = r;
-    tp.kslices = (K + lora::kTSlice - 1) / lora::kTSlice;
-    tp.tpart = reinterpret_cast<float*>(wsb + wl.tpart);
-    tp.tcount = reinterpret_cast<unsigned long long*>(wsb + wl.tcount);
-    tp.epoch = epoch;
+    tp.ngroups = ngroups;
+    tp.R64 = R64;
+    const int rt = ngroups * r;
+    tp.nj = rt <= 64 ? 2 : 8;
+    tp.col_blocks = std::max(1, (rt + 8 * tp.nj - 1) / (8 * tp.nj));
     tp.t64 = t;
     tp.b64 = b64;
-    const int tblocks = (Ms + lora::kTRows - 1) / lora::kTRows * tp.kslices;
-    const int bblocks = (N + lora::kTThreads - 1) / lora::kTThreads;
-    lora::lora_t_kernel<<<tblocks + bblocks, lora::kTThreads, 0, stream>>>(tp);
-    if (cudaGetLastError() != cudaSuccess) return IDLM_ERR_CUDA;
+    if (r > 0) {
+      const int tblocks = (Ms + lora::kTRows - 1) / lora::kTRows * tp.col_blocks;
+      const int bblocks = pad_b ? (N + lora::kTThreads - 1) / lora::kTThreads : 0;
+      lora::lora_t_kernel<<<tblocks + bblocks, lora::kTThreads, 0, stream>>>(tp);
+      if (cudaGetLastError() != cudaSuccess) return IDLM_ERR_CUDA;
+    }
 
     lora::Params p;
     p.y = yb + static_cast<size_t>(m0) * N;
-    p.part = reinterpret_cast<float*>(wsb + wl.part);
-    p.flag = reinterpret_cast<unsigned long long*>(wsb + wl.flag);
-    p.epoch = epoch;
-    // Failure-detection test switch: with IDLM_TEST_STALE_FLAGS=1 a finaliser
-    // waits for a flag value that no CTA writes, so its bounded wait runs out
-    // (after 20 ms) and the call ends with TIMEOUT in the status word.
-    const char* stale = std::getenv("IDLM_TEST_STALE_FLAGS");
-    const bool stale_test = stale && stale[0] == '1';
-    p.wait_epoch = stale_test ? epoch + 1 : epoch;
-    p.flag_wait_ns = stale_test ? 20000000ull : kWaitNs;
+    p.part = reinterpret_cast<float4*>(wsb + wl.part);
     p.status = status;
     p.M = Ms;
     p.N = N;
@@ -945,17 +979,25 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
     p.n2 = pl.n2;
     p.tiles = pl.tiles;
     p.kb = pl.kb;
+    p.nad = pl.nad;
     p.S = pl.S;
-    p.U = pl.U;
+    p.sk_tiles = pl.sk_tiles;
+    p.dp_per = pl.dp_per;
+    p.U_sk = pl.U_sk;
+    p.ngroups = ngroups;
+    for (int g = 0; g < lora::kMaxGroups; ++g)
+      p.group_end[g] = g < ngroups ? (gend_rows[g] + lora::kTileN - 1) / lora::kTileN : pl.tiles;
+    p.R64 = R64;
     p.stages = stages;
     p.nacc = pl.nacc;
     p.yvec = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0) ? 1 : 0;
     const size_t ring = size_t(stages) * pl.stage_bytes;
     const size_t ytile_bytes = size_t(pl.m16) * lora::kTileN * 2;
-    p.ytma = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0) ? 1 : 0;
-    p.ytile_off = static_cast<uint32_t>(p.ytma ? (ring - ytile_bytes) / 1024 * 1024 : ring);
-    p.pslots = std::min<int>(lora::kMaxPSlots, static_cast<int>(p.ytile_off / lora::kPiece));
-    if (p.pslots < 1) return IDLM_ERR_UNSUPPORTED;
+    p.ytma = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0 && ytile_bytes <= ring) ? 1 : 0;
+    p.ytile_off = static_cast<uint32_t>(p.ytma ? (ring - ytile_bytes) / 1024 * 1024 : 0);
+    p.stage_bytes = pl.stage_bytes;
+    p.wait_ns = test_stall ? 20000000ull : kWaitNs;
+    p.test_stall = test_stall ? 1 : 0;
     CUtensorMap ym;
     if (p.ytma) {
       const uint64_t ydims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(Ms)};
@@ -965,10 +1007,6 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
     } else {
       ym = wm;   // unused
     }
-    p.stage_bytes = pl.stage_bytes;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.grid);
     cfg.blockDim = dim3(lora::kThreads);
@@ -983,6 +1021,63 @@ extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void*
       e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, wm, xm1, xm2, bm, tm1, tm2, ym, p);
     }
     if (e != cudaSuccess) return IDLM_ERR_CUDA;
+    if (pl.U_sk > 0) {
+      lora::FParams f;
+      f.part = p.part;
+      f.y = p.y;
+      f.U_sk = pl.U_sk;
+      f.S = pl.S;
+      f.G = pl.grid;
+      f.M = Ms;
+      f.N = N;
+      f.m16 = pl.m16;
+      f.sk_tiles = pl.sk_tiles;
+      cudaLaunchConfig_t fc = {};
+      fc.gridDim = dim3(pl.sk_tiles * ((pl.m16 + 31) / 32));
+      fc.blockDim = dim3(128);
+      fc.stream = stream;
+      fc.attrs = at;
+      fc.numAttrs = 1;
+      e = cudaLaunchKernelEx(&fc, lora::lora_fixup_kernel, f);
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        fc.numAttrs = 0;
+        e = cudaLaunchKernelEx(&fc, lora::lora_fixup_kernel, f);
+      }
+      if (e != cudaSuccess) return IDLM_ERR_CUDA;
+    }
   }
   return IDLM_OK;
+}
+
+}  // namespace
+
+extern "C" size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r) {
+  if (M <= 0 || K <= 0 || N <= 0 || r < 0) return 0;
+  return ws_layout(M, N, r, 1).total;
+}
+
+extern "C" size_t idlm_gated_lora_grouped_workspace_size(int M, int K, int N, int r, int ngroups) {
+  if (M <= 0 || K <= 0 || N <= 0 || r < 0 || ngroups < 1) return 0;
+  return ws_layout(M, N, r, ngroups).total;
+}
+
+extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void* lora_a,
+                                       const void* lora_b, const uint8_t* row_gate,
+                                       float lora_scale, int M, int K, int N, int r, void* y,
+                                       void* workspace, size_t workspace_bytes, int32_t* status,
+                                       void* stream) {
+  return gated_lora_impl(x, w, lora_a, lora_b, row_gate, lora_scale, M, K, N, r, 1, nullptr, y,
+                         workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" idlm_status idlm_gated_lora_grouped(const void* x, const void* w, const void* lora_a,
+                                               const void* lora_b, const uint8_t* row_gate,
+                                               float lora_scale, int M, int K, int N, int r,
+                                               int ngroups, const int* group_rows, void* y,
+                                               void* workspace, size_t workspace_bytes,
+                                               int32_t* status, void* stream) {
+  return gated_lora_impl(x, w, lora_a, lora_b, row_gate, lora_scale, M, K, N, r, ngroups,
+                         group_rows, y, workspace, workspace_bytes, status,
+                         static_cast<cudaStream_t>(stream));
 }

@@ -227,7 +227,7 @@ def accept_inputs(w, seed=0):
         targets=targets, sigma=sig, temperature=w.temperature)
 
 
-def lora_inputs(w, seed=0):
+def lora_inputs(w, seed=0, rank=None):
     """Weights and activations of one decoder layer's seven projections.
 
     Projections (K -> N): q 4096->4096, k 4096->1024, v 4096->1024,
@@ -237,7 +237,8 @@ def lora_inputs(w, seed=0):
     request's 2N-1 rows), 0 elsewhere.
     """
     g = _gen(seed + 2)
-    H, F, r = w.hidden, w.ffn, w.lora_rank
+    H, F = w.hidden, w.ffn
+    r = w.lora_rank if rank is None else rank
     kvd = w.Hkv * w.D
     shapes = dict(q=(H, H), k=(kvd, H), v=(kvd, H), o=(H, H), gate=(F, H),
                   up=(F, H), down=(H, F))
@@ -251,7 +252,7 @@ def lora_inputs(w, seed=0):
             b=(torch.randn(n, r, generator=g) * 0.02).bfloat16())
     pos = torch.arange(M) % (2 * w.N - 1)
     row_gate = (pos >= w.N).to(torch.uint8)
-    return dict(x=x, proj=proj, row_gate=row_gate, lora_scale=1.0)
+    return dict(x=x, proj=proj, row_gate=row_gate, lora_scale=1.0, rank=r)
 
 
 def fuse_projections(proj, names):
@@ -272,3 +273,127 @@ def fuse_projections(proj, names):
         r0 += b.shape[1]
     return dict(w=W, a=A, b=B)
 
+
+
+# ---------------------------------------------------------------------------
+# Synthetic model for multi-step loops: logit rows as a function of
+# (request, slot, step).  The same definition runs on the GPU in
+# idlm_synth_logits; this is its CPU twin (bit-identical by construction).
+# ---------------------------------------------------------------------------
+
+PHILOX32_M = (0xD2511F53, 0xCD9E8D57)
+PHILOX32_W = (0x9E3779B9, 0xBB67AE85)
+SYNTH_KEY1 = 0x1D1A7E5D
+IH8_CENTRE = 4 * 65535
+
+
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) on numpy arrays.
+
+    ctr: four counter words (ints or uint32-valued arrays, broadcast
+    together); key: two key words.  Returns four uint64 arrays holding the
+    32-bit output words."""
+    import numpy as np
+    m32 = np.uint64(0xFFFFFFFF)
+    c0, c1, c2, c3 = np.broadcast_arrays(*[np.asarray(x, dtype=np.uint64) & m32 for x in ctr])
+    k0, k1 = (np.uint64(int(k) & 0xFFFFFFFF) for k in key)
+    for r in range(10):
+        if r:
+            k0 = (k0 + np.uint64(PHILOX32_W[0])) & m32
+            k1 = (k1 + np.uint64(PHILOX32_W[1])) & m32
+        p0 = c0 * np.uint64(PHILOX32_M[0])
+        p1 = c2 * np.uint64(PHILOX32_M[1])
+        c0, c1, c2, c3 = (((p1 >> np.uint64(32)) ^ c1 ^ k0) & m32, p1 & m32,
+                          ((p0 >> np.uint64(32)) ^ c3 ^ k1) & m32, p0 & m32)
+    return c0, c1, c2, c3
+
+
+def ih8(words):
+    """Centred sum of the eight 16-bit halves of four 32-bit words (int64)."""
+    import numpy as np
+    s = np.zeros(np.shape(words[0]), dtype=np.int64)
+    for w in words:
+        w = w.astype(np.int64)
+        s += (w & 0xFFFF) + (w >> 16)
+    return s - IH8_CENTRE
+
+
+def synth_scale(std):
+    """fp32 factor that turns a centred IH8 sum into a value of standard
+    deviation `std` (the sum's variance is (2/3) 65536^2)."""
+    import numpy as np
+    return float(np.float32(std * math.sqrt(1.5) / 65536.0))
+
+
+def f32_to_bf16_bits(x):
+    """Round float32 values to bfloat16, nearest-even (finite values)."""
+    import numpy as np
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return b.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b):
+    import numpy as np
+    return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
+
+
+def synth_rows(req, pos, is_mask, V, scale_z, scale_e, seed, step):
+    """Logit rows of the synthetic model (bf16 bits, uint16 [rows, V]).
+
+    Row i of request req[i] at position pos[i] predicts slot pos[i] + 1; a
+    clean row holds z(c, s) = fp32(IH8(c, s, 0)) * scale_z, a MASK row
+    z(c, s) + fp32(IH8(c, s, 1 + step)) * scale_e[c], where IH8(c, s, d) is
+    the centred sum of the halves of Philox4x32-10(counter = (v, s, c, d),
+    key = (seed, 0x1D1A7E5D)).  Products and the sum are rounded to nearest
+    in fp32, the result to nearest-even in bf16."""
+    import numpy as np
+    req = np.asarray(req, dtype=np.int64)
+    pos = np.asarray(pos, dtype=np.int64)
+    v = np.arange(V, dtype=np.uint64)[None, :]
+    slot = (pos + 1).astype(np.uint64)[:, None]
+    c = req.astype(np.uint64)[:, None]
+    key = (seed, SYNTH_KEY1)
+    sz = ih8(philox4x32_10((v, slot, c, 0), key))
+    x = sz.astype(np.float32) * np.float32(scale_z)
+    mask = np.asarray(is_mask, dtype=bool)
+    if mask.any():
+        rows = np.nonzero(mask)[0]
+        sn = ih8(philox4x32_10((v, slot[rows], c[rows], 1 + int(step)), key))
+        se = np.asarray(scale_e, dtype=np.float32)[req[rows]][:, None]
+        x[rows] = x[rows] + sn.astype(np.float32) * se
+    return f32_to_bf16_bits(x)
+
+
+
+def layer_inputs(w, rank=None, seed=0, requests=None):
+    """A whole decoder layer of the gated-LoRA workload, stacked the way
+    idlm_risd_layer takes it: w_qkv = [Wq; Wk; Wv], a_qkv = [Aq; Ak; Av],
+    b_qkv = [Bq; Bk; Bv], w_gu = [Wgate; Wup], a_gu, b_gu; plus the step's
+    rows (x, MASK gate) and the attention's paged KV (the workload's contexts).
+    rank overrides the adapters' rank (0: no adapters).  requests: keep only
+    these requests' rows and KV (a smaller batch of the same layer)."""
+    inp = lora_inputs(w, seed=seed, rank=rank if rank else (w.lora_rank if rank is None else 8))
+    P = inp["proj"]
+    cat = lambda names, key: torch.cat([P[n][key] for n in names])
+    W = dict(w_qkv=cat("qkv", "w"), a_qkv=cat("qkv", "a"), b_qkv=cat("qkv", "b"),
+             w_o=P["o"]["w"], a_o=P["o"]["a"], b_o=P["o"]["b"],
+             w_gu=cat(("gate", "up"), "w"), a_gu=cat(("gate", "up"), "a"),
+             b_gu=cat(("gate", "up"), "b"),
+             w_down=P["down"]["w"], a_down=P["down"]["a"], b_down=P["down"]["b"])
+    if rank == 0:
+        for k in [k for k in W if k[0] in "ab"]:
+            del W[k]
+    a = attention_inputs(w, seed=seed)
+    x, gate = inp["x"], inp["row_gate"]
+    if requests is not None:
+        qo = a["qo_indptr"]
+        rows = torch.cat([torch.arange(int(qo[c]), int(qo[c + 1])) for c in requests])
+        sub_qo = torch.zeros(len(requests) + 1, dtype=torch.int32)
+        sub_qo[1:] = torch.cumsum(torch.tensor([int(qo[c + 1] - qo[c]) for c in requests]), 0)
+        a = dict(a, page_table=a["page_table"][list(requests)], seq_lens=a["seq_lens"][list(requests)],
+                 qo_indptr=sub_qo)
+        x, gate = x[rows], gate[rows]
+    return dict(W=W, x=x, row_gate=gate, rank=0 if rank == 0 else inp["rank"],
+                k_cache=a["k_cache"], v_cache=a["v_cache"], page_table=a["page_table"],
+                seq_lens=a["seq_lens"], qo_indptr=a["qo_indptr"], lora_scale=1.0)

@@ -84,14 +84,15 @@ def test_gated_lora_host_checks_without_a_gpu(lib):
     odd = ctypes.c_void_p(264)    # 8-byte aligned only
     ws = lib.idlm_gated_lora_workspace_size(448, 4096, 1024, 16)
     assert ws > 0
-    # null pointers
+    # null pointers (the adapter's may be null only at rank 0)
     assert lib.idlm_gated_lora(None, d, d, d, d, 1.0, 448, 4096, 1024, 16, d, d, ws, d, None) == 1
+    assert lib.idlm_gated_lora(d, d, None, d, d, 1.0, 448, 4096, 1024, 16, d, d, ws, d, None) == 1
     assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 16, d, d, ws, None, None) == 1
-    # sizes: M = 0, K not a multiple of 8, r not a multiple of 8 or above 64
+    # sizes: M = 0, K not a multiple of 8, r not a multiple of 8 or above 128
     assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 0, 4096, 1024, 16, d, d, ws, d, None) == 1
     assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4092, 1024, 16, d, d, ws, d, None) == 2
     assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 12, d, d, ws, d, None) == 2
-    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 72, d, d, ws, d, None) == 2
+    assert lib.idlm_gated_lora(d, d, d, d, d, 1.0, 448, 4096, 1024, 136, d, d, ws, d, None) == 2
     # operands must be 16-byte aligned (TMA)
     assert lib.idlm_gated_lora(odd, d, d, d, d, 1.0, 448, 4096, 1024, 16, d, d, ws, d, None) == 1
     # workspace: too small, or not 256-byte aligned
@@ -101,9 +102,28 @@ def test_gated_lora_host_checks_without_a_gpu(lib):
 
 def test_gated_lora_workspace_size(lib):
     f = lib.idlm_gated_lora_workspace_size
-    assert f(0, 4096, 1024, 16) == 0 and f(448, 4096, 1024, 0) == 0
-    # grows with N (the padded B rows) and with K (the adapter's K-slice partials)
+    assert f(0, 4096, 1024, 16) == 0 and f(448, 4096, 1024, -1) == 0
+    # rank 0 (no adapter) is a plain projection: partial tiles only
+    assert 0 < f(448, 4096, 1024, 0) < f(448, 4096, 1024, 16)
+    # grows with N (the padded B rows) and with the rank (the adapter operands)
     assert f(448, 4096, 2048, 16) > f(448, 4096, 1024, 16)
-    assert f(448, 8192, 1024, 16) > f(448, 4096, 1024, 16)
+    assert f(448, 4096, 1024, 72) > f(448, 4096, 1024, 16)
+    g = lib.idlm_gated_lora_grouped_workspace_size
+    assert g(448, 4096, 6144, 16, 1) == f(448, 4096, 6144, 16)
+    assert g(448, 4096, 6144, 16, 3) > g(448, 4096, 6144, 16, 1)
     # token rows beyond one 448-row slice reuse the slice's workspace
     assert f(4480, 4096, 1024, 16) == f(448, 4096, 1024, 16)
+
+
+def test_grouped_gated_lora_host_checks_without_a_gpu(lib):
+    d = ctypes.c_void_p(256)
+    ws = lib.idlm_gated_lora_grouped_workspace_size(448, 4096, 6144, 16, 3)
+    rows = (ctypes.c_int * 3)(4096, 1024, 1024)
+    bad_sum = (ctypes.c_int * 3)(4096, 1024, 1000)
+    unaligned = (ctypes.c_int * 3)(4000, 1120, 1024)
+    f = lib.idlm_gated_lora_grouped
+    assert f(d, d, d, d, d, 1.0, 448, 4096, 6144, 16, 3, None, d, d, ws, d, None) == 1
+    assert f(d, d, d, d, d, 1.0, 448, 4096, 6144, 16, 3, bad_sum, d, d, ws, d, None) == 1
+    assert f(d, d, d, d, d, 1.0, 448, 4096, 6144, 16, 3, unaligned, d, d, ws, d, None) == 2
+    assert f(d, d, d, d, d, 1.0, 448, 4096, 6144, 16, 5, rows, d, d, ws, d, None) == 2
+    assert f(d, d, d, d, d, 1.0, 448, 4096, 6144, 16, 3, rows, d, d, ws - 1, d, None) == 3

@@ -169,17 +169,79 @@ def test_fused_projections_match_the_separate_ones(cuda_device):
 
 def test_a_wait_that_runs_out_reports_timeout_and_the_context_survives(cuda_device, monkeypatch):
     """Failure detection without a GPU fault.  Under the test switch
-    IDLM_TEST_STALE_FLAGS=1 a CTA that adds the partial sums of a split tile
-    waits for a flag value that no CTA ever writes; its bounded wait (20 ms)
-    runs out, the kernel records TIMEOUT (5) in the status word, drains its
-    copies, frees its tensor memory and returns.  The next call, without the
-    switch, must run normally and match the oracle."""
+    IDLM_TEST_STALL=1 every GEMM CTA first waits on an mbarrier that nothing
+    arrives on; its bounded wait (20 ms) runs out, the kernel records
+    TIMEOUT (5) in the status word, drains its copies, frees its tensor
+    memory and returns.  The next call, without the switch, must run
+    normally and match the oracle."""
     x, w, a, b, g = case(64, 1024, 256, 16, seed=13)
     monkeypatch.setenv("IDLM_LORA_GRID", "7")   # 2 tiles x 17 K steps over 7 CTAs: split
-    monkeypatch.setenv("IDLM_TEST_STALE_FLAGS", "1")
+    monkeypatch.setenv("IDLM_TEST_STALL", "1")
     _, st = gpu_lora_status(x, w, a, b, g, 1.0)
     assert st == 5, f"expected TIMEOUT, device status {st}"
-    monkeypatch.delenv("IDLM_TEST_STALE_FLAGS")
+    monkeypatch.delenv("IDLM_TEST_STALL")
     y = gpu_lora(x, w, a, b, g, 1.0)
     ref = isd.gated_lora(f64(x), f64(w), f64(a), f64(b), g.numpy(), 1.0)
     assert_close(f64(y), ref)
+
+
+@pytest.mark.parametrize("M,K,N,r", [(448, 1024, 384, 72), (448, 4096, 512, 128),
+                                     (37, 320, 200, 128), (130, 2048, 256, 120)])
+def test_rank_up_to_128_matches_the_oracle(cuda_device, M, K, N, r):
+    """Ranks above 64 take two adapter K steps ("Lossless R-ISD": the pages'
+    adapter has rank 128)."""
+    x, w, a, b, g = case(M, K, N, r, seed=r + K)
+    y = gpu_lora(x, w, a, b, g, 1.0)
+    ref = isd.gated_lora(f64(x), f64(w), f64(a), f64(b), g.numpy(), 1.0)
+    assert_close(f64(y), ref)
+
+
+def test_rank_128_ungated_rows_bit_identical(cuda_device, monkeypatch):
+    monkeypatch.setenv("IDLM_LORA_GRID", "37")
+    x, w, a, b, g = case(448, 2048, 640, 128, seed=21, wstd=0.2)
+    y = gpu_lora(x, w, a, b, g, 1.0)
+    y0 = gpu_lora(x, w, a, torch.zeros_like(b), g, 1.0)
+    clean = (g == 0).cuda()
+    assert torch.equal(y[clean], y0[clean])
+    assert not torch.equal(y[~clean], y0[~clean])
+
+
+def gpu_lora_grouped(x, w, a, b, g, s, group_rows, dev="cuda"):
+    M, K = x.shape
+    N = w.shape[0]
+    r = a.shape[0] // len(group_rows)
+    ws = torch.empty(lib.idlm_gated_lora_grouped_workspace_size(M, K, N, r, len(group_rows)),
+                     dtype=torch.uint8, device=dev)
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.idlm_gated_lora_grouped(x.to(dev), w.to(dev), a.to(dev), b.to(dev), g.to(dev), s,
+                                group_rows, y, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    return y
+
+
+@pytest.mark.parametrize("r", [16, 128])
+def test_grouped_projections_match_the_separate_ones(cuda_device, r):
+    """q|k|v in one call with one adapter per group: each group's columns
+    match that projection's own call and the oracle, within the tolerance
+    (the two calls may split their K sums differently)."""
+    gen = torch.Generator().manual_seed(r)
+    M, K = 448, 1024
+    rows = [512, 256, 256]
+    x = torch.randn(M, K, generator=gen).bfloat16()
+    g = (torch.arange(M) % 7 >= 4).to(torch.uint8)
+    ws_, as_, bs_ = [], [], []
+    for n in rows:
+        ws_.append((torch.randn(n, K, generator=gen) * 0.02).bfloat16())
+        as_.append((torch.randn(r, K, generator=gen) * 0.02).bfloat16())
+        bs_.append((torch.randn(n, r, generator=gen) * 0.02).bfloat16())
+    W, A, B = torch.cat(ws_), torch.cat(as_), torch.cat(bs_)
+    yg = f64(gpu_lora_grouped(x, W, A, B, g, 1.0, rows))
+    n0 = 0
+    for i, n in enumerate(rows):
+        ys = f64(gpu_lora(x, ws_[i], as_[i], bs_[i], g, 1.0))
+        assert_close(yg[:, n0:n0 + n], ys)
+        ref = isd.gated_lora(f64(x), f64(ws_[i]), f64(as_[i]), f64(bs_[i]), g.numpy(), 1.0)
+        assert_close(yg[:, n0:n0 + n], ref)
+        n0 += n

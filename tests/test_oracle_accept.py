@@ -253,3 +253,54 @@ def test_bad_row_layout_is_rejected():
     with pytest.raises(ValueError):
         isd.isd_accept(np.zeros((5, 4)), np.array([0, 5]), np.array([1]), np.zeros((1, 2), int),
                        np.zeros((2, 4)), np.array([0]), 4, 1.0, 0, 0, 0)
+
+
+def test_decode_positions_feed_each_slot_its_own_rows():
+    """isd_decode(with_positions=True) gives the model every row's absolute
+    position.  With the slot-indexed synthetic model of the workloads, a
+    draft is proposed from the MASK row of its slot at one step and verified
+    against the clean row of the same slot at the next, so in SAMPLE mode
+    the realised acceptance equals the mean overlap sum_v min(p_v, q_v) of
+    those row pairs; a position off by one would pair unrelated rows."""
+    from speculative_verify_accept_step_b300 import workloads as wl
+    C, N, V, steps, seed = 300, 4, 256, 8, 2
+    sz = wl.synth_scale(2.0)
+    se = np.full(C, wl.synth_scale(0.6), dtype=np.float32)
+    step = [0]
+    tested = accepted = 0
+
+    def model(row_tok, row_req, row_mask_k, row_last_clean, row_pos):
+        bits = wl.synth_rows(row_req, row_pos, row_tok == isd.MASK_TOKEN, V, sz, se, seed,
+                             step[0])
+        step[0] += 1
+        return wl.bf16_bits_to_f32(bits).astype(np.float64)
+
+    outs = []
+    orig = isd.isd_accept
+
+    def traced(*a, **k):
+        o = orig(*a, **k)
+        outs.append(o)
+        return o
+    isd.isd_accept = traced
+    try:
+        start = np.arange(C) % 50
+        isd.isd_decode(model, np.zeros(C, dtype=np.int64), N, steps, 1.0, isd.PROPOSE_SAMPLE,
+                       seed, start_len=start, with_positions=True)
+    finally:
+        isd.isd_accept = orig
+    for o in outs:
+        full = o["final_kind"] != isd.END_FRESH
+        n = o["n_accepted"][full]
+        tested += int(np.minimum(n + 1, N - 1).sum())
+        accepted += int(n.sum())
+    p_hat = accepted / tested
+    # expected overlap of a slot's MASK row (some step) with its clean row
+    slots = np.arange(400) + 7
+    req = np.arange(400) % C
+    p = wl.bf16_bits_to_f32(wl.synth_rows(req, slots, np.zeros(400, bool), V, sz, se, seed, 0))
+    q = wl.bf16_bits_to_f32(wl.synth_rows(req, slots, np.ones(400, bool), V, sz, se, seed, 0))
+    overlap = np.minimum(isd.softmax_t(p.astype(np.float64), 1.0),
+                         isd.softmax_t(q.astype(np.float64), 1.0)).sum(-1).mean()
+    assert 0.3 < overlap < 0.95
+    assert abs(p_hat - overlap) < 0.02, (p_hat, overlap)

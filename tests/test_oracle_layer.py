@@ -1,0 +1,110 @@
+"""Pins of the oracle's decoder layer pieces (CPU only): RMSNorm and SiLU
+against hand values and closed forms, the grouped projection against its
+groups, and two properties of the whole layer -- all-zero weights leave the
+residual stream untouched, and clean rows never see the MASK rows'
+adapters ("Lossless R-ISD": verify positions keep the base model's output)."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import isd
+
+
+def test_rmsnorm_hand_values_and_invariances():
+    y = isd.rmsnorm(np.array([[3.0, 4.0]]), 0.0)
+    r = math.sqrt((9 + 16) / 2)
+    np.testing.assert_allclose(y, [[3 / r, 4 / r]], rtol=1e-15)
+    # a constant vector maps to +-1 (eps = 0), then times the weight
+    np.testing.assert_allclose(isd.rmsnorm(np.full((1, 5), -2.5), 0.0), -np.ones((1, 5)))
+    w = np.arange(1.0, 6.0)
+    np.testing.assert_allclose(isd.rmsnorm(np.full((1, 5), 7.0), 0.0, w), w[None])
+    # scale invariance without eps; eps shrinks small vectors toward 0
+    x = np.random.default_rng(0).standard_normal((3, 64))
+    np.testing.assert_allclose(isd.rmsnorm(5 * x, 0.0), isd.rmsnorm(x, 0.0), rtol=1e-12)
+    assert np.abs(isd.rmsnorm(1e-6 * x, 1e-6)).max() < 1e-2
+
+
+def test_silu_hand_values():
+    np.testing.assert_allclose(isd.silu([0.0, 1.0, -1.0]),
+                               [0.0, 1 / (1 + math.exp(-1)), -1 / (1 + math.e)], rtol=1e-15)
+    assert abs(isd.silu(40.0) - 40.0) < 1e-12 and abs(isd.silu(-40.0)) < 1e-15
+
+
+def test_round_bf16_keeps_eight_bits():
+    assert isd.round_bf16(1.0) == 1.0
+    assert isd.round_bf16(1 + 2 ** -8) == 1.0           # half an ulp: ties to even
+    assert isd.round_bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6
+    assert isd.round_bf16(-3.14159) == -3.140625
+
+
+def test_grouped_projection_is_its_groups():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((6, 16))
+    rows, r = [8, 4, 4], 2
+    w = rng.standard_normal((16, 16))
+    a = rng.standard_normal((3 * r, 16))
+    b = rng.standard_normal((16, r))
+    g = np.array([0, 1, 0, 1, 1, 0])
+    y = isd.gated_lora_grouped(x, w, a, b, g, 0.5, rows)
+    n0 = 0
+    for i, n in enumerate(rows):
+        want = x @ w[n0:n0 + n].T + 0.5 * g[:, None] * (x @ a[i * r:(i + 1) * r].T) @ b[n0:n0 + n].T
+        np.testing.assert_allclose(y[:, n0:n0 + n], want, rtol=1e-12, atol=1e-12)
+        n0 += n
+
+
+def _layer_case(rank, seed=0, zero=False, C=3, N=4, H=32, F=64, Hq=4, Hkv=2, D=8, P=4):
+    rng = np.random.default_rng(seed)
+    rows = 2 * N - 1
+    T = C * rows
+    nq, nkv = Hq * D, Hkv * D
+    s = 0.0 if zero else 0.2
+    W = dict(w_qkv=s * rng.standard_normal((nq + 2 * nkv, H)),
+             a_qkv=rng.standard_normal((3 * rank, H)), b_qkv=rng.standard_normal((nq + 2 * nkv, rank)),
+             w_o=s * rng.standard_normal((H, nq)), a_o=rng.standard_normal((rank, nq)),
+             b_o=(0 if zero else 1) * rng.standard_normal((H, rank)),
+             w_gu=s * rng.standard_normal((2 * F, H)), a_gu=rng.standard_normal((2 * rank, H)),
+             b_gu=rng.standard_normal((2 * F, rank)),
+             w_down=s * rng.standard_normal((H, F)), a_down=rng.standard_normal((rank, F)),
+             b_down=(0 if zero else 1) * rng.standard_normal((H, rank)),
+             norm1=None, norm2=None)
+    lens = np.array([0, 5, 13])[:C]
+    need = [(L + rows + P - 1) // P for L in lens]
+    table = np.full((C, max(need)), -1)
+    at = 0
+    for c, n in enumerate(need):
+        table[c, :n] = np.arange(at, at + n)
+        at += n
+    kc = rng.standard_normal((at, Hkv, P, D))
+    vc = rng.standard_normal((at, Hkv, P, D))
+    qo = np.arange(0, T + 1, rows)
+    gate = (np.arange(T) % rows >= N).astype(np.int64)
+    x = rng.standard_normal((T, H))
+    args = dict(n_heads=Hq, n_kv_heads=Hkv, head_dim=D, k_cache=kc, v_cache=vc, page_table=table,
+                seq_lens=lens, qo_indptr=qo, page_size=P)
+    return x, W, gate, args
+
+
+def test_zero_weights_leave_the_residual_stream():
+    x, W, gate, args = _layer_case(4, zero=True)
+    out, _, _ = isd.risd_layer(x, W, gate, 1.0, 1e-6, **args)
+    # attention output meets Wo = 0 and B_o = 0; silu(0) * 0 = 0 meets Wd = 0
+    assert np.array_equal(out, x)
+
+
+@pytest.mark.parametrize("rank", [2, 8])
+def test_clean_rows_do_not_see_the_adapters(rank):
+    x, W, gate, args = _layer_case(rank, seed=rank)
+    out, _, _ = isd.risd_layer(x, W, gate, 1.0, 1e-6, **args)
+    # the same layer with every adapter's B = 0 (the same arithmetic, the
+    # adapter term exactly zero everywhere)
+    W0 = dict(W)
+    for k in ("b_qkv", "b_o", "b_gu", "b_down"):
+        W0[k] = np.zeros_like(W[k])
+    base, _, _ = isd.risd_layer(x, W0, gate, 1.0, 1e-6, **args)
+    clean = gate == 0
+    # a clean row's whole computation: row-wise ops on itself and causal
+    # attention over the clean rows before it; the adapters touch MASK rows only
+    assert np.array_equal(out[clean], base[clean])
+    assert np.abs(out[~clean] - base[~clean]).max() > 1e-3

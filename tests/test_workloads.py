@@ -69,3 +69,40 @@ def test_fused_projections_are_exact():
                          + (x @ inp["proj"][n]["a"].double().T) @ inp["proj"][n]["b"].double().T
                          for n in names], 1)
         assert torch.equal(fused, sep) or float((fused - sep).abs().max()) < 1e-12
+
+
+# ------------------------------------------------- synthetic model for loops
+
+def test_philox4x32_known_answers():
+    """Philox4x32-10 against the generator authors' published known-answer
+    vectors (Random123 distribution, kat_vectors: philox4x32 with 10 rounds)."""
+    cases = [((0, 0, 0, 0), (0, 0), (0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8)),
+             ((0xffffffff,) * 4, (0xffffffff,) * 2,
+              (0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd)),
+             ((0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344), (0xa4093822, 0x299f31d0),
+              (0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1))]
+    for ctr, key, want in cases:
+        got = wl.philox4x32_10(ctr, key)
+        assert tuple(int(x) for x in got) == want
+
+
+def test_synth_rows_moments_and_slot_consistency():
+    import numpy as np
+    V = 8192
+    sz = wl.synth_scale(3.0)
+    se = np.array([wl.synth_scale(0.5)], dtype=np.float32)
+    clean = wl.bf16_bits_to_f32(wl.synth_rows([0] * 4, [10, 11, 12, 13], [False] * 4, V, sz, se,
+                                              3, 0)).astype(np.float64)
+    assert abs(clean.mean()) < 0.05 and abs(clean.std() - 3.0) < 0.05
+    # the same slot at another step: clean rows identical, MASK rows differ by
+    # noise of the requested scale
+    again = wl.bf16_bits_to_f32(wl.synth_rows([0], [11], [False], V, sz, se, 3, 7))
+    assert np.array_equal(again[0], clean[1].astype(np.float32))
+    m5 = wl.bf16_bits_to_f32(wl.synth_rows([0], [11], [True], V, sz, se, 3, 5)).astype(np.float64)
+    m6 = wl.bf16_bits_to_f32(wl.synth_rows([0], [11], [True], V, sz, se, 3, 6)).astype(np.float64)
+    d5, d6 = m5[0] - clean[1], m6[0] - clean[1]
+    assert abs(d5.std() - 0.5) < 0.03 and abs(d6.std() - 0.5) < 0.03
+    assert abs(np.corrcoef(d5, d6)[0, 1]) < 0.05
+    # another request, same slot: independent values
+    other = wl.bf16_bits_to_f32(wl.synth_rows([1], [11], [False], V, sz, se, 3, 0))
+    assert abs(np.corrcoef(other[0], clean[1])[0, 1]) < 0.05
