@@ -378,22 +378,26 @@ def kv_commit(k_cache, v_cache, page_table, seq_lens, k_new, v_new, qo_indptr,
 # a3: gated LoRA (R-ISD)
 # ---------------------------------------------------------------------------
 
-def gated_lora(x, w, lora_a, lora_b, row_gate, lora_scale):
+def gated_lora(x, w, lora_a, lora_b, row_gate, lora_scale, store=None):
     """Y = X W^T + g * s * (X A^T) B^T with g = 1 only at MASK rows.
 
     [IDLM] "Lossless R-ISD" / [GN] "Speedup Factor Explorer": the LoRA adapter
     is active only at MASK positions; verify positions use the base weights
     alone, so their outputs equal the base model's bit for bit.
     x: [M, K], w: [N, K], lora_a: [r, K], lora_b: [N, r], row_gate: [M].
+    store: the rounding applied to the rank-r intermediate T = g s X A^T
+    where an implementation stores it (None: exact float64).
     """
     x = np.asarray(x, dtype=np.float64)
     base = x @ np.asarray(w, dtype=np.float64).T
     t = x @ np.asarray(lora_a, dtype=np.float64).T
     t = t * (np.asarray(row_gate, dtype=np.float64)[:, None] * lora_scale)
+    if store is not None:
+        t = store(t)
     return base + t @ np.asarray(lora_b, dtype=np.float64).T
 
 
-def gated_lora_grouped(x, w, lora_a, lora_b, row_gate, lora_scale, group_rows):
+def gated_lora_grouped(x, w, lora_a, lora_b, row_gate, lora_scale, group_rows, store=None):
     """Several gated-LoRA projections of one input with stacked weights.
 
     Group g owns weight rows [sum(group_rows[:g]), sum(group_rows[:g+1]));
@@ -406,7 +410,7 @@ def gated_lora_grouped(x, w, lora_a, lora_b, row_gate, lora_scale, group_rows):
     outs, n0 = [], 0
     for g, n in enumerate(group_rows):
         outs.append(gated_lora(x, np.asarray(w)[n0:n0 + n], np.asarray(lora_a)[g * r:(g + 1) * r],
-                               np.asarray(lora_b)[n0:n0 + n], row_gate, lora_scale))
+                               np.asarray(lora_b)[n0:n0 + n], row_gate, lora_scale, store))
         n0 += n
     return np.concatenate(outs, axis=1)
 
@@ -446,7 +450,8 @@ def risd_layer(x, W, row_gate, lora_scale, eps, n_heads, n_kv_heads, head_dim,
     w_o [H, Hq D], a_o, b_o, w_gu [2F, H] (gate rows, then up rows), a_gu
     [2r, H], b_gu, w_down [H, F], a_down, b_down, norm1, norm2 ([H] or None);
     rank 0 means no adapters (a_* of zero rows).  store: the rounding applied
-    where an implementation stores an activation (None: exact float64).
+    where an implementation stores an activation, the adapters' rank-r
+    intermediates included (None: exact float64).
 
         n1 = RMSNorm(x)               h  = x + a Wo^T (+ LoRA)
         [q|k|v] = n1 Wqkv^T (+ LoRA)  n2 = RMSNorm(h)
@@ -463,7 +468,7 @@ def risd_layer(x, W, row_gate, lora_scale, eps, n_heads, n_kv_heads, head_dim,
     def proj(inp, w, a, b, rows):
         if np.asarray(a).shape[0] == 0:
             return np.asarray(inp, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
-        return gated_lora_grouped(inp, w, a, b, row_gate, lora_scale, rows)
+        return gated_lora_grouped(inp, w, a, b, row_gate, lora_scale, rows, store)
 
     n1 = st(rmsnorm(x, eps, W.get("norm1")))
     qkv = st(proj(n1, W["w_qkv"], W["a_qkv"], W["b_qkv"], [nq, nkv, nkv]))

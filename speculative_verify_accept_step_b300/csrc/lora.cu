@@ -44,6 +44,8 @@
 // IDLM_DEV_TIMEOUT, and the CTA drains its copies and MMAs and frees its
 // tensor memory before it leaves.
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdlib>
 #include <mutex>
 
@@ -273,20 +275,21 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
 
 // ------------------------------------------------------------------ T = g s X A^T
 //
-// One CTA per block of 16 token rows x NJ*8 adapter columns (columns of all
-// groups, concatenated) with the whole K; its 8 warps take one eighth of K
-// each and accumulate with mma.sync (m16n8k16, bf16 in, fp32 accumulate),
-// then add their sums in warp order.  T = g s (X A^T) is stored in bf16 at
-// T64[m][group * R64 + j], zeros at gated-off rows and in the padding
-// columns j >= r.  Extra CTAs copy B to 64-value blocks (zeros past r)
-// where r % 64 != 0.
+// T [M x rt] (rt = groups * r adapter columns) is a small product with a
+// long K, so each CTA takes a block of 16 token rows x CB <= 64 columns and
+// one slice of K: it stages its X rows and A rows for the slice in shared
+// memory with 1-D bulk copies (every row in flight at once), then its 8
+// warps (one 8-column MMA tile each) run mma.sync m16n8k16 (bf16 in, fp32
+// accumulate) over the slice from shared memory.  Slices are summed in slice
+// order by the last CTA of the (rows, columns) block to finish (an arrival
+// counter tagged with the launch's epoch, so the workspace needs no
+// clearing).  T = g s (X A^T) is stored in bf16 at T64[m][group * R64 + j],
+// zeros at gated-off rows and in the padding columns j >= r.  Extra CTAs
+// copy B to 64-value blocks (zeros past r) where r % 64 != 0.
 constexpr int kTRows = 16;
 constexpr int kTThreads = 256;
 constexpr int kTWarps = kTThreads / 32;
-
-__device__ __forceinline__ uint32_t ldg32(const __nv_bfloat16* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
-}
+constexpr int kTMaxCols = 64;
 
 struct TParams {
   const __nv_bfloat16* x;
@@ -295,79 +298,136 @@ struct TParams {
   const uint8_t* gate;
   float scale;
   int M, K, N, r, ngroups, R64;
-  int nj;                       // 8-column MMA tiles per block (2 or 8)
-  int col_blocks;               // ceil(ngroups * r / (8 nj))
+  int rt;                       // ngroups * r
+  int cb;                       // columns per CTA (multiple of 8, <= 64)
+  int col_blocks, row_blocks, kslices, kl;   // kl: K per slice (multiple of 16)
+  float* tpart;                 // [row_blocks * col_blocks][kslices][16][cb] fp32
+  unsigned long long* tcount;   // [row_blocks * col_blocks]: epoch << 32 | slices done
+  unsigned long long epoch;
+  int32_t* status;
   __nv_bfloat16* t64;           // [M, ngroups * R64]
   __nv_bfloat16* b64;           // [N, R64]
 };
 
-template <int NJ>
-__device__ void t_block(const TParams& p, int m0, int j0) {
-  __shared__ float red[kTWarps][kTRows][8 * NJ];
-  __shared__ int any_gate;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rt = p.ngroups * p.r;
-  if (tid == 0) any_gate = 0;
-  __syncthreads();
-  if (tid < kTRows && m0 + tid < p.M && p.gate[m0 + tid]) atomicOr(&any_gate, 1);
-  __syncthreads();
-  const int g = lane >> 2, t4 = lane & 3;
-  float acc[NJ][4];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-  if (any_gate) {
-    const bool r0 = m0 + g < p.M, r1 = m0 + g + 8 < p.M;
-    const __nv_bfloat16* x0 = p.x + static_cast<size_t>(r0 ? m0 + g : 0) * p.K;
-    const __nv_bfloat16* x1 = p.x + static_cast<size_t>(r1 ? m0 + g + 8 : 0) * p.K;
-    const __nv_bfloat16* arow[NJ];
-    bool aval[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int col = j0 + j * 8 + g;
-      aval[j] = col < rt;
-      arow[j] = p.a + static_cast<size_t>(aval[j] ? col : 0) * p.K;
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+__global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
+  extern __shared__ uint8_t tsm_raw[];
+  __shared__ uint64_t bar;
+  __shared__ int last;
+  __shared__ float red[kTRows][kTMaxCols];
+  const int tblocks = p.row_blocks * p.col_blocks * p.kslices;
+  if (static_cast<int>(blockIdx.x) >= tblocks) {
+    // B -> B64: row n, 64-value blocks, zeros past r
+    const int n = (blockIdx.x - tblocks) * kTThreads + threadIdx.x;
+    if (n < p.N) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.b + static_cast<size_t>(n) * p.r);
+      uint4* dst = reinterpret_cast<uint4*>(p.b64 + static_cast<size_t>(n) * p.R64);
+      for (int q = 0; q < p.R64 / 8; ++q) dst[q] = q < p.r / 8 ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
     }
-    const int kper = (p.K + kTWarps * 16 - 1) / (kTWarps * 16) * 16;   // K per warp, 16s
-    const int kbeg = warp * kper, kend = min(p.K, kbeg + kper);
-#pragma unroll 2
-    for (int k16 = kbeg; k16 < kend; k16 += 16) {
-      const int k = k16 + 2 * t4;
-      const bool lo = k < p.K, hi = k + 8 < p.K;   // K % 8 == 0: pairs never straddle K
-      uint32_t af[4];
-      af[0] = (r0 && lo) ? ldg32(x0 + k) : 0u;
-      af[1] = (r1 && lo) ? ldg32(x1 + k) : 0u;
-      af[2] = (r0 && hi) ? ldg32(x0 + k + 8) : 0u;
-      af[3] = (r1 && hi) ? ldg32(x1 + k + 8) : 0u;
-      uint32_t bf[NJ][2];
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        bf[j][0] = (aval[j] && lo) ? ldg32(arow[j] + k) : 0u;
-        bf[j][1] = (aval[j] && hi) ? ldg32(arow[j] + k + 8) : 0u;
-      }
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) mma_bf16_16816(acc[j], af, bf[j][0], bf[j][1]);
+    return;
+  }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int blk = blockIdx.x / p.kslices, ks = blockIdx.x % p.kslices;
+  const int rb = blk / p.col_blocks, cbk = blk % p.col_blocks;
+  const int m0 = rb * kTRows, j0 = cbk * p.cb;
+  const int k0 = ks * p.kl, kl = min(p.kl, p.K - k0);   // K % 8 == 0, kl % 8 == 0
+  const int kl16 = (kl + 15) / 16 * 16;
+  const int stride = (p.kl + 8) * 2;                    // bytes per staged row (16-byte pad)
+  uint8_t* xs = tsm_raw + ((16 - (smem_u32(tsm_raw) & 15)) & 15);
+  uint8_t* as = xs + kTRows * stride;
+  const int nrows = min(kTRows, p.M - m0);
+  const int ncols = min(p.cb, p.rt - j0);
+  // zero what the copies do not cover: rows past M or rt, and the K tail
+  // of every row up to the next multiple of 16
+  for (int e = tid; e < (kTRows + p.cb) * ((p.kl + 8) / 8); e += kTThreads) {
+    const int row = e / ((p.kl + 8) / 8), c8 = (e % ((p.kl + 8) / 8)) * 8;
+    const bool real = row < kTRows ? row < nrows : (row - kTRows) < ncols;
+    if (!real || c8 >= kl)
+      *reinterpret_cast<uint4*>((row < kTRows ? xs + row * stride : as + (row - kTRows) * stride) +
+                                c8 * 2) = make_uint4(0, 0, 0, 0);
+  }
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>((nrows + ncols) * kl * 2));
+    for (int i = 0; i < nrows; ++i)
+      bulk_g2s(xs + i * stride, p.x + static_cast<size_t>(m0 + i) * p.K + k0, kl * 2, &bar);
+    for (int j = 0; j < ncols; ++j)
+      bulk_g2s(as + j * stride, p.a + static_cast<size_t>(j0 + j) * p.K + k0, kl * 2, &bar);
+  }
+  const bool ok = mbar_wait_bounded(&bar, 0, nullptr, p.status);
+  // warp w: output columns j0 + 8w .. 8w + 7
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (ok && warp * 8 < ncols) {
+    const uint32_t xb = smem_u32(xs), ab = smem_u32(as + warp * 8 * stride);
+    const int xr = lane & 15, xc = (lane >> 4) * 8;       // x4: rows 0-15, k 0-7 / 8-15
+    const int ar = lane & 7, ac = ((lane >> 3) & 1) * 8;  // x2: rows 0-7, k 0-7 / 8-15
+    for (int k = 0; k < kl16; k += 16) {
+      uint32_t a4[4], b0, b1;
+      ldsm_x4(xb + xr * stride + (k + xc) * 2, a4[0], a4[1], a4[2], a4[3]);
+      ldsm_x2(ab + ar * stride + (k + ac) * 2, b0, b1);
+      mma_bf16_16816(acc, a4, b0, b1);
     }
   }
-  // the warps' sums, added in warp order
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    red[warp][g][8 * j + 2 * t4] = acc[j][0];
-    red[warp][g][8 * j + 2 * t4 + 1] = acc[j][1];
-    red[warp][g + 8][8 * j + 2 * t4] = acc[j][2];
-    red[warp][g + 8][8 * j + 2 * t4 + 1] = acc[j][3];
+  // acc: rows g and g + 8, columns 2 t4, 2 t4 + 1 of the warp's 8
+  const int g = lane >> 2, t4 = lane & 3;
+  const size_t tile = static_cast<size_t>(kTRows) * p.cb;
+  float* mine = p.tpart + (static_cast<size_t>(blk) * p.kslices + ks) * tile;
+  if (warp * 8 < p.cb) {
+    const int c = warp * 8 + 2 * t4;
+    if (p.kslices == 1) {
+      red[g][c] = acc[0];
+      red[g][c + 1] = acc[1];
+      red[g + 8][c] = acc[2];
+      red[g + 8][c + 1] = acc[3];
+    } else {
+      __stcg(mine + g * p.cb + c, acc[0]);
+      __stcg(mine + g * p.cb + c + 1, acc[1]);
+      __stcg(mine + (g + 8) * p.cb + c, acc[2]);
+      __stcg(mine + (g + 8) * p.cb + c + 1, acc[3]);
+    }
+  }
+  if (p.kslices > 1) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const unsigned long long tag = (p.epoch & 0xffffffffull) << 32;
+      unsigned long long* cnt = p.tcount + blk;
+      unsigned long long seen, old = *reinterpret_cast<volatile unsigned long long*>(cnt);
+      do {
+        seen = old;
+        const unsigned long long nv = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
+        old = atomicCAS(cnt, seen, nv);
+      } while (old != seen);
+      const unsigned long long now = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
+      last = (now & 0xffffffffull) == static_cast<unsigned long long>(p.kslices);
+      __threadfence();
+    }
+    __syncthreads();
+    if (!last) return;
+    // the slices in slice order
+    const float* base = p.tpart + static_cast<size_t>(blk) * p.kslices * tile;
+    for (int e = tid; e < kTRows * p.cb; e += kTThreads) {
+      float v = 0.f;
+      for (int q = 0; q < p.kslices; ++q) v += __ldcg(base + q * tile + e);
+      red[e / p.cb][e % p.cb] = v;
+    }
   }
   __syncthreads();
   const size_t tstride = static_cast<size_t>(p.ngroups) * p.R64;
-  for (int e = tid; e < kTRows * NJ * 8; e += kTThreads) {
-    const int i = e / (NJ * 8), cl = e % (NJ * 8);
+  for (int e = tid; e < kTRows * p.cb; e += kTThreads) {
+    const int i = e / p.cb, cl = e % p.cb;
     const int m = m0 + i, col = j0 + cl;
-    if (m >= p.M || col >= rt) continue;
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kTWarps; ++w) v += red[w][i][cl];
-    v = p.gate[m] ? v * p.scale : 0.f;
+    if (m >= p.M || col >= p.rt) continue;
+    const float v = p.gate[m] ? red[i][cl] * p.scale : 0.f;
     const int grp = col / p.r, jj = col % p.r;
     p.t64[static_cast<size_t>(m) * tstride + grp * p.R64 + jj] = __float2bfloat16_rn(v);
   }
@@ -380,28 +440,28 @@ __device__ void t_block(const TParams& p, int m0, int j0) {
       const int grp = rem / pad, jj = p.r + rem % pad;
       const int m = m0 + i;
       const int last_col = grp * p.r + p.r - 1;
-      if (m < p.M && last_col >= j0 && last_col < j0 + NJ * 8)
+      if (m < p.M && last_col >= j0 && last_col < j0 + p.cb)
         p.t64[static_cast<size_t>(m) * tstride + grp * p.R64 + jj] = __float2bfloat16_rn(0.f);
     }
   }
 }
 
-__global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
-  const int groups = (p.M + kTRows - 1) / kTRows;
-  const int tblocks = groups * p.col_blocks;
-  if (static_cast<int>(blockIdx.x) >= tblocks) {
-    // B -> B64: row n, 64-value blocks, zeros past r
-    const int n = (blockIdx.x - tblocks) * kTThreads + threadIdx.x;
-    if (n < p.N) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.b + static_cast<size_t>(n) * p.r);
-      uint4* dst = reinterpret_cast<uint4*>(p.b64 + static_cast<size_t>(n) * p.R64);
-      for (int q = 0; q < p.R64 / 8; ++q) dst[q] = q < p.r / 8 ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
-    }
-    return;
+// The adapter kernel's split of T over CTAs: CB columns per CTA, K slices so
+// that about one CTA per SM works and a CTA's staged rows fit in shared
+// memory.  Returns the dynamic shared memory per CTA.
+inline size_t t_plan(int M, int K, int rt, int sms, int& cb, int& col_blocks, int& row_blocks,
+                     int& kslices, int& kl) {
+  col_blocks = (rt + kTMaxCols - 1) / kTMaxCols;
+  cb = ((rt + col_blocks - 1) / col_blocks + 7) / 8 * 8;
+  row_blocks = (M + kTRows - 1) / kTRows;
+  const int base = row_blocks * col_blocks;
+  kslices = std::max(1, std::min(sms / base, (K + 255) / 256));
+  for (;;) {
+    kl = ((K + kslices - 1) / kslices + 15) / 16 * 16;
+    const size_t smem = 16 + static_cast<size_t>(kTRows + cb) * (kl + 8) * 2;
+    if (smem <= 160 * 1024 || kl <= 256) return smem;
+    ++kslices;
   }
-  const int grp = blockIdx.x / p.col_blocks, cb = blockIdx.x % p.col_blocks;
-  if (p.nj == 8) t_block<8>(p, grp * kTRows, cb * 64);
-  else t_block<2>(p, grp * kTRows, cb * 16);
 }
 
 // ------------------------------------------------------------ the GEMM
@@ -769,17 +829,21 @@ int max_grid() {
 int r64_of(int r) { return (r + lora::kPadW - 1) / lora::kPadW * lora::kPadW; }
 
 struct WsLayout {
-  size_t t64, b64, part, total;
+  size_t t64, b64, tpart, tcount, part, total;
 };
-WsLayout ws_layout(int M, int N, int r, int ngroups) {
+WsLayout ws_layout(int M, int K, int N, int r, int ngroups) {
   const int Ms = std::min(M, lora::kMaxTokens);
   const size_t m16 = (Ms + 15) / 16 * 16;
   const size_t G = max_grid();
   const size_t R64 = r64_of(r);
+  int cb = 8, cbl = 1, rbl = 1, ks = 1, kl = 16;
+  if (r > 0) lora::t_plan(Ms, K, ngroups * r, static_cast<int>(G), cb, cbl, rbl, ks, kl);
   WsLayout l;
   l.t64 = 0;
   l.b64 = align_up(static_cast<size_t>(Ms) * ngroups * R64 * 2, 256);
-  l.part = l.b64 + align_up(static_cast<size_t>(N) * R64 * 2, 256);
+  l.tpart = l.b64 + align_up(static_cast<size_t>(N) * R64 * 2, 256);
+  l.tcount = l.tpart + align_up(static_cast<size_t>(rbl) * cbl * ks * lora::kTRows * cb * 4, 256);
+  l.part = l.tcount + align_up(static_cast<size_t>(rbl) * cbl * 8, 256);
   l.total = l.part + G * 2 * lora::kTileN * m16 * sizeof(float);
   return l;
 }
@@ -870,7 +934,7 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
        reinterpret_cast<uintptr_t>(lora_a) | reinterpret_cast<uintptr_t>(lora_b)) & 15)
     return IDLM_ERR_INVALID_ARG;
-  const WsLayout wl = ws_layout(M, N, r, ngroups);
+  const WsLayout wl = ws_layout(M, K, N, r, ngroups);
   if (!workspace || workspace_bytes < wl.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return IDLM_ERR_WORKSPACE;
   DeviceInfo dev;
@@ -883,7 +947,9 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
     if (dev.device < 0 || dev.device >= 64) return IDLM_ERR_CUDA;
     if (done[dev.device] != ctx || ctx == 0) {
       if (cudaFuncSetAttribute(lora::lora_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dev.max_smem_optin) != cudaSuccess)
+                               dev.max_smem_optin) != cudaSuccess ||
+          cudaFuncSetAttribute(lora::lora_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024) != cudaSuccess)
         return IDLM_ERR_CUDA;
       done[dev.device] = ctx;
     }
@@ -943,27 +1009,35 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
       return IDLM_ERR_CUDA;
     }
 
-    lora::TParams tp;
-    tp.x = xs;
-    tp.a = static_cast<const __nv_bfloat16*>(lora_a);
-    tp.b = static_cast<const __nv_bfloat16*>(lora_b);
-    tp.gate = row_gate + m0;
-    tp.scale = lora_scale;
-    tp.M = Ms;
-    tp.K = K;
-    tp.N = N;
-    tp.r = r;
-    tp.ngroups = ngroups;
-    tp.R64 = R64;
-    const int rt = ngroups * r;
-    tp.nj = rt <= 64 ? 2 : 8;
-    tp.col_blocks = std::max(1, (rt + 8 * tp.nj - 1) / (8 * tp.nj));
-    tp.t64 = t;
-    tp.b64 = b64;
     if (r > 0) {
-      const int tblocks = (Ms + lora::kTRows - 1) / lora::kTRows * tp.col_blocks;
+      // launches get distinct epochs, so the slice counters never need clearing
+      static std::atomic<unsigned long long> epoch_counter{
+          0x9e3779b97f4a7c15ull ^
+          static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};
+      lora::TParams tp;
+      tp.x = xs;
+      tp.a = static_cast<const __nv_bfloat16*>(lora_a);
+      tp.b = static_cast<const __nv_bfloat16*>(lora_b);
+      tp.gate = row_gate + m0;
+      tp.scale = lora_scale;
+      tp.M = Ms;
+      tp.K = K;
+      tp.N = N;
+      tp.r = r;
+      tp.ngroups = ngroups;
+      tp.R64 = R64;
+      tp.rt = ngroups * r;
+      const size_t tsmem = lora::t_plan(Ms, K, tp.rt, grid_cap, tp.cb, tp.col_blocks,
+                                        tp.row_blocks, tp.kslices, tp.kl);
+      tp.tpart = reinterpret_cast<float*>(wsb + wl.tpart);
+      tp.tcount = reinterpret_cast<unsigned long long*>(wsb + wl.tcount);
+      tp.epoch = ++epoch_counter;
+      tp.status = status;
+      tp.t64 = t;
+      tp.b64 = b64;
+      const int tblocks = tp.row_blocks * tp.col_blocks * tp.kslices;
       const int bblocks = pad_b ? (N + lora::kTThreads - 1) / lora::kTThreads : 0;
-      lora::lora_t_kernel<<<tblocks + bblocks, lora::kTThreads, 0, stream>>>(tp);
+      lora::lora_t_kernel<<<tblocks + bblocks, lora::kTThreads, tsmem, stream>>>(tp);
       if (cudaGetLastError() != cudaSuccess) return IDLM_ERR_CUDA;
     }
 
@@ -1054,12 +1128,12 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
 
 extern "C" size_t idlm_gated_lora_workspace_size(int M, int K, int N, int r) {
   if (M <= 0 || K <= 0 || N <= 0 || r < 0) return 0;
-  return ws_layout(M, N, r, 1).total;
+  return ws_layout(M, K, N, r, 1).total;
 }
 
 extern "C" size_t idlm_gated_lora_grouped_workspace_size(int M, int K, int N, int r, int ngroups) {
   if (M <= 0 || K <= 0 || N <= 0 || r < 0 || ngroups < 1) return 0;
-  return ws_layout(M, N, r, ngroups).total;
+  return ws_layout(M, K, N, r, ngroups).total;
 }
 
 extern "C" idlm_status idlm_gated_lora(const void* x, const void* w, const void* lora_a,
