@@ -2,10 +2,18 @@
 oracle's layer (marked gpu).
 
 The oracle stores every activation in bf16 where the library does (the
-workload is a bf16 layer), computing each step in float64; the comparison
-uses the bf16 bound |gpu - oracle| <= 2e-2 + 1e-2 |oracle|.  Clean rows
-must equal the same layer without adapters (every B = 0) bit for bit:
-causal attention keeps MASK rows out of clean rows ("Lossless R-ISD").
+workload is a bf16 layer, the adapters' rank-r intermediates included),
+computing each step in float64.  A layer chains eleven stored activations;
+where the GPU's fp32 and the oracle's float64 land on either side of a bf16
+rounding edge, an element differs by one ulp and the difference travels
+through the later ops.  The tolerance is derived from that: flipping 1% of
+every stored activation of the oracle by one ulp moves its outputs by up to
+2.4 times the single-op bound 2e-2 + 1e-2 |x| (measured in
+tests/test_oracle_layer.py, which also pins this), so each element must be
+within 4 times that bound, and the mean error within a quarter of the
+bound's mean (1% flips give 0.15 - 0.2).  Clean rows must equal the same layer without adapters (every B = 0)
+bit for bit: causal attention keeps MASK rows out of clean rows ("Lossless
+R-ISD").
 """
 import math
 
@@ -16,10 +24,12 @@ import torch
 import speculative_verify_accept_step_b300 as lib
 from oracle import isd
 from speculative_verify_accept_step_b300 import workloads as wl
+from _layer_cases import small_case
 
 pytestmark = pytest.mark.gpu
 
-ATOL, RTOL = 2e-2, 1e-2
+ATOL, RTOL = 2e-2, 1e-2       # the single-op bf16 bound
+LAYER_FACTOR = 4.0              # chained bf16 activations (see the module docstring)
 
 
 def f64(t):
@@ -62,40 +72,13 @@ def oracle_layer(inp, Hq, Hkv, D, eps=1e-6):
                           inp["qo_indptr"].numpy(), 16, store=isd.round_bf16)
 
 
-def assert_close(got, ref):
+def assert_close(got, ref, factor=LAYER_FACTOR):
     err = np.abs(got - ref)
     bound = ATOL + RTOL * np.abs(ref)
     worst = float((err / bound).max())
-    assert np.all(err <= bound), f"worst err/bound {worst:.3f}"
+    assert np.all(err <= factor * bound), f"worst err/bound {worst:.3f}"
+    assert err.mean() <= 0.25 * bound.mean(), f"mean err {err.mean():.4g}"
     return worst
-
-
-def small_case(rank, seed, Hq=8, Hkv=2, D=64, H=512, F=1024, C=4, N=4):
-    g = torch.Generator().manual_seed(seed)
-    rows = 2 * N - 1
-    nq, nkv = Hq * D, Hkv * D
-    mk = lambda *s: (torch.randn(*s, generator=g) * 0.05).bfloat16()
-    W = dict(w_qkv=mk(nq + 2 * nkv, H), w_o=mk(H, nq), w_gu=mk(2 * F, H), w_down=mk(H, F))
-    if rank:
-        W.update(a_qkv=mk(3 * rank, H), b_qkv=mk(nq + 2 * nkv, rank), a_o=mk(rank, nq),
-                 b_o=mk(H, rank), a_gu=mk(2 * rank, H), b_gu=mk(2 * F, rank), a_down=mk(rank, F),
-                 b_down=mk(H, rank))
-    lens = [0, 17, 100, 260][:C]
-    P = 16
-    need = [(L + rows + P - 1) // P for L in lens]
-    perm = torch.randperm(sum(need), generator=g)
-    table = torch.full((C, max(need)), -1, dtype=torch.int32)
-    at = 0
-    for c, n in enumerate(need):
-        table[c, :n] = perm[at:at + n].to(torch.int32)
-        at += n
-    T = C * rows
-    return dict(W=W, x=torch.randn(T, H, generator=g).bfloat16(),
-                row_gate=(torch.arange(T) % rows >= N).to(torch.uint8),
-                k_cache=torch.randn(at, Hkv, P, D, generator=g).bfloat16(),
-                v_cache=torch.randn(at, Hkv, P, D, generator=g).bfloat16(),
-                page_table=table, seq_lens=torch.tensor(lens, dtype=torch.int32),
-                qo_indptr=torch.arange(0, T + 1, rows, dtype=torch.int32), lora_scale=1.0)
 
 
 @pytest.mark.parametrize("rank", [0, 16, 128])

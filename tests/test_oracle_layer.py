@@ -108,3 +108,40 @@ def test_clean_rows_do_not_see_the_adapters(rank):
     # attention over the clean rows before it; the adapters touch MASK rows only
     assert np.array_equal(out[clean], base[clean])
     assert np.abs(out[~clean] - base[~clean]).max() > 1e-3
+
+
+def test_layer_tolerance_covers_one_ulp_rounding_flips():
+    """The GPU layer check (tests/test_gpu_layer.py, same case) allows 4 x
+    the single-op bf16 bound per element.  Justification: an implementation
+    computing in fp32 lands on the other side of a bf16 rounding edge for a
+    small fraction of stored values; here 1% of every stored activation of
+    the oracle is moved by one bf16 ulp, and the outputs stay within
+    4 x (2e-2 + 1e-2 |x|) of the unperturbed oracle, with a mean error below
+    a quarter of the bound's mean."""
+    from _layer_cases import small_case
+    for rank in (0, 16, 128):
+        inp = small_case(rank, seed=rank + 1)
+        f = lambda t: t.float().numpy().astype(np.float64)
+        W = {k: f(v) for k, v in inp["W"].items()}
+        for k in ("a_qkv", "a_o", "a_gu", "a_down"):
+            W.setdefault(k, np.zeros((0, 1)))
+        for k in ("b_qkv", "b_o", "b_gu", "b_down"):
+            W.setdefault(k, np.zeros((1, 0)))
+        args = dict(n_heads=8, n_kv_heads=2, head_dim=64, k_cache=f(inp["k_cache"]),
+                    v_cache=f(inp["v_cache"]), page_table=inp["page_table"].numpy(),
+                    seq_lens=inp["seq_lens"].numpy(), qo_indptr=inp["qo_indptr"].numpy(),
+                    page_size=16)
+        x, gate = f(inp["x"]), inp["row_gate"].numpy()
+        ref, _, _ = isd.risd_layer(x, W, gate, 1.0, 1e-6, store=isd.round_bf16, **args)
+        rng = np.random.default_rng(rank)
+
+        def flip(a):
+            r = isd.round_bf16(a)
+            m = rng.random(r.shape) < 0.01
+            step = np.abs(r) * 2.0 ** -8 * np.sign(rng.standard_normal(r.shape))
+            return np.where(m, isd.round_bf16(r + step), r)
+        pert, _, _ = isd.risd_layer(x, W, gate, 1.0, 1e-6, store=flip, **args)
+        bound = 2e-2 + 1e-2 * np.abs(ref)
+        err = np.abs(pert - ref)
+        assert (err / bound).max() < 4.0
+        assert err.mean() < 0.25 * bound.mean()
