@@ -96,7 +96,14 @@ struct Params {
   uint32_t stage_bytes;   // one stage: the weight block, then the token rows
   unsigned long long wait_ns;   // limit of one bounded wait
   int test_stall;         // failure-detection test switch (see the entry point)
+  const uint8_t* rs_gate; // or null: Y row m is scaled by (rs_gate[m] ? rs_scale : 0)
+  float rs_scale;
 };
+
+// Factor of token row m of Y (1 without row scaling).
+__device__ __forceinline__ float row_factor(const uint8_t* gate, float scale, int m) {
+  return gate ? (gate[m] ? scale : 0.f) : 1.f;
+}
 
 // A CTA's work, in order: the segments of its share of the split units, then
 // its whole tiles.  The producer, the MMA issuer and the epilogue walk the
@@ -356,13 +363,14 @@ __global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
     fence_barrier_init();
   }
   __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>((nrows + ncols) * kl * 2));
-    for (int i = 0; i < nrows; ++i)
-      bulk_g2s(xs + i * stride, p.x + static_cast<size_t>(m0 + i) * p.K + k0, kl * 2, &bar);
-    for (int j = 0; j < ncols; ++j)
-      bulk_g2s(as + j * stride, p.a + static_cast<size_t>(j0 + j) * p.K + k0, kl * 2, &bar);
-  }
+  if (tid == 0) mbar_arrive_expect_tx(&bar, static_cast<uint32_t>((nrows + ncols) * kl * 2));
+  __syncthreads();
+  // one row per thread, every copy in flight at once
+  if (tid < nrows)
+    bulk_g2s(xs + tid * stride, p.x + static_cast<size_t>(m0 + tid) * p.K + k0, kl * 2, &bar);
+  else if (tid >= kTRows && tid - kTRows < ncols)
+    bulk_g2s(as + (tid - kTRows) * stride, p.a + static_cast<size_t>(j0 + tid - kTRows) * p.K + k0,
+             kl * 2, &bar);
   const bool ok = mbar_wait_bounded(&bar, 0, nullptr, p.status);
   // warp w: output columns j0 + 8w .. 8w + 7
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -491,7 +499,9 @@ __device__ __noinline__ void store_y_direct(const Params& p, uint32_t taddr, int
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        ystage[j * kTileN + row] = __float2bfloat16_rn(__uint_as_float(ra[16 * h + j]));
+        ystage[j * kTileN + row] = __float2bfloat16_rn(
+            __uint_as_float(ra[16 * h + j]) *
+            row_factor(p.rs_gate, p.rs_scale, min(c0 + 16 * h + j, p.M - 1)));
       epi_sync();
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
@@ -524,7 +534,9 @@ __device__ __noinline__ void store_y_tma(const Params& p, uint32_t taddr, int n_
     tmem_ld_wait(ra);
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (c0 + j < p.m16) ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(__uint_as_float(ra[j]));
+      if (c0 + j < p.m16)
+        ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(
+            __uint_as_float(ra[j]) * row_factor(p.rs_gate, p.rs_scale, min(c0 + j, p.M - 1)));
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
@@ -758,6 +770,8 @@ struct FParams {
   __nv_bfloat16* y;
   long long U_sk;
   int S, G, M, N, m16, sk_tiles;
+  const uint8_t* rs_gate;   // row scaling as in Params
+  float rs_scale;
 };
 
 __device__ __forceinline__ long long fx_begin(const FParams& f, int c) {
@@ -803,7 +817,9 @@ __global__ void __launch_bounds__(128) lora_fixup_kernel(const FParams f) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int m = ch * 32 + j;
-    if (m < f.M) f.y[static_cast<size_t>(m) * f.N + n] = __float2bfloat16_rn(v[j]);
+    if (m < f.M)
+      f.y[static_cast<size_t>(m) * f.N + n] =
+          __float2bfloat16_rn(v[j] * row_factor(f.rs_gate, f.rs_scale, m));
   }
 }
 
@@ -909,6 +925,119 @@ LoraPlan plan_for(int M, int K, int N, int r, int grid_cap) {
   return pl;
 }
 
+struct GemmArgs {
+  const __nv_bfloat16* xs;
+  int Ms, K;
+  const void* w;
+  int N, r, ngroups;
+  const int* gend_rows;
+  int R64;
+  CUtensorMap wm, xm1, xm2, bm, tm1, tm2;
+  __nv_bfloat16* y;         // [Ms, N]
+  float4* part;
+  const uint8_t* rs_gate;   // or null
+  float rs_scale;
+  bool test_stall;
+};
+
+// One GEMM launch over a slice of <= 448 token rows, then the fix-up kernel
+// if the plan splits tiles.
+idlm_status launch_gemm(const GemmArgs& a, const LoraPlan& pl, int stages, size_t smem,
+                        int32_t* status, cudaStream_t stream) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  const int N = a.N;
+  lora::Params p;
+  p.y = a.y;
+  p.part = a.part;
+  p.status = status;
+  p.rs_gate = a.rs_gate;
+  p.rs_scale = a.rs_scale;
+  p.M = a.Ms;
+  p.N = N;
+  p.r = a.r;
+  p.m16 = pl.m16;
+  p.n1 = pl.n1;
+  p.n2 = pl.n2;
+  p.tiles = pl.tiles;
+  p.kb = pl.kb;
+  p.nad = pl.nad;
+  p.S = pl.S;
+  p.sk_tiles = pl.sk_tiles;
+  p.dp_per = pl.dp_per;
+  p.U_sk = pl.U_sk;
+  p.ngroups = a.ngroups;
+  for (int g = 0; g < lora::kMaxGroups; ++g)
+    p.group_end[g] =
+        g < a.ngroups ? (a.gend_rows[g] + lora::kTileN - 1) / lora::kTileN : pl.tiles;
+  p.R64 = a.R64;
+  p.stages = stages;
+  p.nacc = pl.nacc;
+  const bool yok = N % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0;
+  p.yvec = yok ? 1 : 0;
+  const size_t ring = size_t(stages) * pl.stage_bytes;
+  const size_t ytile_bytes = size_t(pl.m16) * lora::kTileN * 2;
+  p.ytma = (yok && ytile_bytes <= ring) ? 1 : 0;
+  p.ytile_off = static_cast<uint32_t>(p.ytma ? (ring - ytile_bytes) / 1024 * 1024 : 0);
+  p.stage_bytes = pl.stage_bytes;
+  p.wait_ns = a.test_stall ? 20000000ull : kWaitNs;
+  p.test_stall = a.test_stall ? 1 : 0;
+  CUtensorMap ym;
+  if (p.ytma) {
+    const uint64_t ydims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(a.Ms)};
+    const uint64_t ystr[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t ybox[2] = {lora::kTileN, lora::kYBoxRows};
+    if (!encode_bf16_map(&ym, p.y, 2, ydims, ystr, ybox, 0)) return IDLM_ERR_CUDA;
+  } else {
+    ym = a.wm;   // unused
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(lora::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, a.wm, a.xm1, a.xm2, a.bm,
+                                     a.tm1, a.tm2, ym, p);
+  if (e != cudaSuccess) {   // without programmatic dependent launch
+    (void)cudaGetLastError();
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, a.wm, a.xm1, a.xm2, a.bm, a.tm1, a.tm2,
+                           ym, p);
+  }
+  if (e != cudaSuccess) return IDLM_ERR_CUDA;
+  if (pl.U_sk > 0) {
+    lora::FParams f;
+    f.part = p.part;
+    f.y = p.y;
+    f.U_sk = pl.U_sk;
+    f.S = pl.S;
+    f.G = pl.grid;
+    f.M = a.Ms;
+    f.N = N;
+    f.m16 = pl.m16;
+    f.sk_tiles = pl.sk_tiles;
+    f.rs_gate = a.rs_gate;
+    f.rs_scale = a.rs_scale;
+    cudaLaunchConfig_t fc = {};
+    fc.gridDim = dim3(pl.sk_tiles * ((pl.m16 + 31) / 32));
+    fc.blockDim = dim3(128);
+    fc.stream = stream;
+    fc.attrs = at;
+    fc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&fc, lora::lora_fixup_kernel, f);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      fc.numAttrs = 0;
+      e = cudaLaunchKernelEx(&fc, lora::lora_fixup_kernel, f);
+    }
+    if (e != cudaSuccess) return IDLM_ERR_CUDA;
+  }
+  return IDLM_OK;
+}
+
 idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, const void* lora_b,
                             const uint8_t* row_gate, float lora_scale, int M, int K, int N, int r,
                             int ngroups, const int* group_rows, void* y, void* workspace,
@@ -968,9 +1097,6 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
   const int grid_cap = std::min(dev.sm_count, max_grid());
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
   // token rows in slices of at most 448 (the tensor-memory columns and the ring)
   for (int m0 = 0; m0 < M; m0 += lora::kMaxTokens) {
     const int Ms = std::min(lora::kMaxTokens, M - m0);
@@ -1009,7 +1135,24 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
       return IDLM_ERR_CUDA;
     }
 
-    if (r > 0) {
+    if (r > 0 && R64 == r) {
+      // r a multiple of 64: T = g s X A^T is itself a projection of X (the
+      // stacked A as weights, [groups * r, K]) with its output rows scaled
+      // by g s, written straight into T64 (no padding columns): the same
+      // tensor-core GEMM, without an adapter.
+      const int rt = ngroups * r;
+      const LoraPlan tpl = plan_for(Ms, K, rt, 0, grid_cap);
+      CUtensorMap am;
+      const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rt)};
+      if (!encode_bf16_map(&am, const_cast<void*>(lora_a), 2, adims, wstr, wbox))
+        return IDLM_ERR_CUDA;
+      const int one[1] = {rt};
+      const GemmArgs ta{xs, Ms, K, lora_a, rt, 0, 1, one, 0, am, xm1, xm2, am, xm1, xm2,
+                        t, reinterpret_cast<float4*>(wsb + wl.part), row_gate + m0, lora_scale,
+                        false};
+      const idlm_status trc = launch_gemm(ta, tpl, stages, smem, status, stream);
+      if (trc != IDLM_OK) return trc;
+    } else if (r > 0) {
       // launches get distinct epochs, so the slice counters never need clearing
       static std::atomic<unsigned long long> epoch_counter{
           0x9e3779b97f4a7c15ull ^
@@ -1041,85 +1184,11 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
       if (cudaGetLastError() != cudaSuccess) return IDLM_ERR_CUDA;
     }
 
-    lora::Params p;
-    p.y = yb + static_cast<size_t>(m0) * N;
-    p.part = reinterpret_cast<float4*>(wsb + wl.part);
-    p.status = status;
-    p.M = Ms;
-    p.N = N;
-    p.r = r;
-    p.m16 = pl.m16;
-    p.n1 = pl.n1;
-    p.n2 = pl.n2;
-    p.tiles = pl.tiles;
-    p.kb = pl.kb;
-    p.nad = pl.nad;
-    p.S = pl.S;
-    p.sk_tiles = pl.sk_tiles;
-    p.dp_per = pl.dp_per;
-    p.U_sk = pl.U_sk;
-    p.ngroups = ngroups;
-    for (int g = 0; g < lora::kMaxGroups; ++g)
-      p.group_end[g] = g < ngroups ? (gend_rows[g] + lora::kTileN - 1) / lora::kTileN : pl.tiles;
-    p.R64 = R64;
-    p.stages = stages;
-    p.nacc = pl.nacc;
-    p.yvec = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0) ? 1 : 0;
-    const size_t ring = size_t(stages) * pl.stage_bytes;
-    const size_t ytile_bytes = size_t(pl.m16) * lora::kTileN * 2;
-    p.ytma = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0 && ytile_bytes <= ring) ? 1 : 0;
-    p.ytile_off = static_cast<uint32_t>(p.ytma ? (ring - ytile_bytes) / 1024 * 1024 : 0);
-    p.stage_bytes = pl.stage_bytes;
-    p.wait_ns = test_stall ? 20000000ull : kWaitNs;
-    p.test_stall = test_stall ? 1 : 0;
-    CUtensorMap ym;
-    if (p.ytma) {
-      const uint64_t ydims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(Ms)};
-      const uint64_t ystr[1] = {static_cast<uint64_t>(N) * 2};
-      const uint32_t ybox[2] = {lora::kTileN, lora::kYBoxRows};
-      if (!encode_bf16_map(&ym, p.y, 2, ydims, ystr, ybox, 0)) return IDLM_ERR_CUDA;
-    } else {
-      ym = wm;   // unused
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.grid);
-    cfg.blockDim = dim3(lora::kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, wm, xm1, xm2, bm, tm1, tm2, ym, p);
-    if (e != cudaSuccess) {   // without programmatic dependent launch
-      (void)cudaGetLastError();
-      cfg.numAttrs = 0;
-      e = cudaLaunchKernelEx(&cfg, lora::lora_gemm_kernel, wm, xm1, xm2, bm, tm1, tm2, ym, p);
-    }
-    if (e != cudaSuccess) return IDLM_ERR_CUDA;
-    if (pl.U_sk > 0) {
-      lora::FParams f;
-      f.part = p.part;
-      f.y = p.y;
-      f.U_sk = pl.U_sk;
-      f.S = pl.S;
-      f.G = pl.grid;
-      f.M = Ms;
-      f.N = N;
-      f.m16 = pl.m16;
-      f.sk_tiles = pl.sk_tiles;
-      cudaLaunchConfig_t fc = {};
-      fc.gridDim = dim3(pl.sk_tiles * ((pl.m16 + 31) / 32));
-      fc.blockDim = dim3(128);
-      fc.stream = stream;
-      fc.attrs = at;
-      fc.numAttrs = 1;
-      e = cudaLaunchKernelEx(&fc, lora::lora_fixup_kernel, f);
-      if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        fc.numAttrs = 0;
-        e = cudaLaunchKernelEx(&fc, lora::lora_fixup_kernel, f);
-      }
-      if (e != cudaSuccess) return IDLM_ERR_CUDA;
-    }
+    const GemmArgs ga{xs, Ms, K, w, N, r, ngroups, gend_rows, R64, wm, xm1, xm2, bm, tm1, tm2,
+                      yb + static_cast<size_t>(m0) * N, reinterpret_cast<float4*>(wsb + wl.part),
+                      nullptr, 0.f, test_stall};
+    const idlm_status rc = launch_gemm(ga, pl, stages, smem, status, stream);
+    if (rc != IDLM_OK) return rc;
   }
   return IDLM_OK;
 }
