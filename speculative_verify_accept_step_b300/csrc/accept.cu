@@ -14,7 +14,7 @@
 //
 // Kernel 1 (vocab_stream_kernel) is the only pass over all logits.  A
 // persistent grid (one CTA per SM) splits the list of 8 KB chunks of all rows
-// evenly; a producer thread streams each CTA's chunks into a 26-stage
+// evenly; a producer thread streams each CTA's chunks into a 22-stage
 // shared-memory ring with 1-D bulk copies (cp.async.bulk, mbarrier
 // completion), and eleven consumer warps each take whole chunks (copied to registers, so
 // the stage is free again at once): packed
@@ -47,8 +47,15 @@ namespace idlm {
 namespace acc {
 
 constexpr int kItemBytes = 8192;                 // one chunk of a row
-constexpr int kStages = 26;                      // kernel-1 ring depth
 constexpr int kCWarps = 11;                      // kernel-1 consumer warps
+// Kernel-1 ring depth, a multiple of kCWarps: consumer warp w takes chunks
+// j = w, w + kCWarps, ..., so stage j % kStages is only ever read by warp w
+// and a warp waits on a stage's next phase only after it consumed the one
+// before.  With another depth, warp w could wait on stage s for chunk j while
+// chunk j - kStages (another warp's) has not landed yet, and the parity test
+// would pass on the older phase.
+constexpr int kStages = 2 * kCWarps;
+static_assert(kStages % kCWarps == 0, "a stage must return to the warp that read it");
 constexpr int kK1Threads = 32 * (kCWarps + 2);   // + producer warp + request warp
 constexpr size_t kK1Smem = 1024 + size_t(kStages) * kItemBytes + 2 * kStages * 8;
 constexpr int kDThreads = 256;                   // decide kernel

@@ -491,7 +491,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
         if (mt == 0 && lane == 0) {
           // CTAs with an empty range (more CTAs than blocks) hold no part.
           // The counter carries this launch's epoch in its high half, so a
-          // count left by an earlier launch reads as zero (no clearing).
+          // count left by an interrupted earlier launch reads as zero.
           int parts = 0;
           for (int b = bf; b <= bl; ++b) parts += range_lo(W, B, b) < range_lo(W, B, b + 1);
           const unsigned long long tag = (p.epoch & 0xffffffffull) << 32;
@@ -506,6 +506,9 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
           const unsigned long long now =
               ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
           flags[1] = (now & 0xffffffffull) == static_cast<unsigned long long>(parts);
+          // the last part clears the counter: a CUDA graph replays this launch
+          // with the same epoch, and must find the count at zero again
+          if (flags[1]) atomicExch(cnt, 0ull);
         }
         named_bar(1 + MT, 32 * MT);
         const bool last = flags[1] != 0;
@@ -688,7 +691,8 @@ idlm_status launch_fast(const DeviceInfo& dev, const void* q, const void* k_new,
   p.ws_o = cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * D);
   p.ws_ml = cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * 2);
   p.ws_cnt = cv.take<unsigned long long>(static_cast<size_t>(C) * Hkv);
-  // launches get distinct epochs, so the merge counters never need clearing
+  // launches get distinct epochs, so a fresh workspace needs no clearing;
+  // the last part of a unit clears its counter for graph replays
   static std::atomic<unsigned long long> epoch_counter{
       0x2545f4914f6cdd1dull ^
       static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};

@@ -289,8 +289,9 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
 // warps (one 8-column MMA tile each) run mma.sync m16n8k16 (bf16 in, fp32
 // accumulate) over the slice from shared memory.  Slices are summed in slice
 // order by the last CTA of the (rows, columns) block to finish (an arrival
-// counter tagged with the launch's epoch, so the workspace needs no
-// clearing).  T = g s (X A^T) is stored in bf16 at T64[m][group * R64 + j],
+// counter tagged with the launch's epoch, so a fresh workspace needs no
+// clearing, and cleared by that last CTA, so a graph replay of the launch
+// finds it at zero).  T = g s (X A^T) is stored in bf16 at T64[m][group * R64 + j],
 // zeros at gated-off rows and in the padding columns j >= r.  Extra CTAs
 // copy B to 64-value blocks (zeros past r) where r % 64 != 0.
 constexpr int kTRows = 16;
@@ -417,6 +418,9 @@ __global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
       } while (old != seen);
       const unsigned long long now = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
       last = (now & 0xffffffffull) == static_cast<unsigned long long>(p.kslices);
+      // the last slice clears the counter: a CUDA graph replays this launch
+      // with the same epoch, and must find the count at zero again
+      if (last) atomicExch(cnt, 0ull);
       __threadfence();
     }
     __syncthreads();
@@ -1153,7 +1157,8 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
       const idlm_status trc = launch_gemm(ta, tpl, stages, smem, status, stream);
       if (trc != IDLM_OK) return trc;
     } else if (r > 0) {
-      // launches get distinct epochs, so the slice counters never need clearing
+      // launches get distinct epochs, so a fresh workspace needs no clearing;
+      // the last slice of a block clears its counter for graph replays
       static std::atomic<unsigned long long> epoch_counter{
           0x9e3779b97f4a7c15ull ^
           static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};

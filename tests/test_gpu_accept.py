@@ -148,3 +148,77 @@ def test_row_layout_mismatch_sets_status(cuda_device):
     out = gpu_accept(l1, b["qo1"].to(dev), torch.zeros(C, dtype=torch.uint8, device=dev), drafts,
                      dq, l1, prow, N, 1.0, 0, 0, 0)
     assert out["status"] == 3
+
+
+def test_more_requests_than_sms(cuda_device):
+    """C = 320 requests over one CTA per SM: a CTA's request warp decides
+    several requests, in the order their chunks finish."""
+    C, N, V = 320, 4, 4096
+    b = _small_batch(C, N, V, seed=21)
+    s0, s1, _ = _check_pair(b, N, 1.0, isd.PROPOSE_ARGMAX, 2, 8)
+    assert s1["compared"] >= C - 8
+
+
+def test_graph_replays_with_new_logits(cuda_device):
+    """One accept launch captured in a CUDA graph and replayed with new logits
+    in its input buffers each time equals an eager call on those logits, bit
+    for bit: the chunk tags of one replay never read as another's."""
+    import speculative_verify_accept_step_b300 as lib
+    from _gpu import alloc_accept, status_tensor
+    C, N, V = 24, 4, 16384
+    dev = "cuda"
+    M = N - 1
+    T = C * (2 * N - 1)
+    qo = torch.arange(0, T + 1, 2 * N - 1, dtype=torch.int32, device=dev)
+    mode = torch.ones(C, dtype=torch.uint8, device=dev)
+    prow = torch.arange(0, C * M, M, dtype=torch.int32, device=dev)
+    logits = torch.empty((T, V), dtype=torch.bfloat16, device=dev)
+    prev = torch.empty((C * M, V), dtype=torch.bfloat16, device=dev)
+    drafts = torch.empty((C, M), dtype=torch.int32, device=dev)
+    dq = torch.empty((C, M, 2), dtype=torch.float32, device=dev)
+
+    def fill(seed):
+        g = torch.Generator().manual_seed(seed)
+        pv = torch.randn(C * M, V, generator=g) * 2
+        lg = torch.randn(T, V, generator=g) * 2
+        for c in range(C):   # verifying rows close to the proposing rows
+            lg[c * (2 * N - 1):c * (2 * N - 1) + M] = pv[c * M:(c + 1) * M] + \
+                0.5 * torch.randn(M, V, generator=g)
+        prev.copy_(pv.bfloat16())
+        logits.copy_(lg.bfloat16())
+        drafts.copy_(prev.float().argmax(-1).reshape(C, M).to(torch.int32))
+        pf = prev.float()
+        m = pf.max(-1).values
+        dq.copy_(torch.stack([m, torch.exp(pf - m[:, None]).sum(-1)], -1).reshape(C, M, 2))
+
+    def call(o, ws, st):
+        lib.idlm_isd_accept(logits, qo, mode, drafts, dq, prev, prow, N, 1.0,
+                            isd.PROPOSE_SAMPLE, 9, 4, o["n_accepted"], o["out_tokens"],
+                            o["n_out"], o["n_commit"], o["next_drafts"], o["next_q_stats"],
+                            o["next_mode"], o["next_mask_row0"], ws, st,
+                            row_stats=o["row_stats"], dbg=o["dbg"])
+
+    size = lib.idlm_isd_accept_workspace_size(C, T, N, V)
+    ws_g = torch.empty(size, dtype=torch.uint8, device=dev)
+    ws_e = torch.empty(size, dtype=torch.uint8, device=dev)
+    og, oe = alloc_accept(C, N, T, dev), alloc_accept(C, N, T, dev)
+    st_g, st_e = status_tensor(dev), status_tensor(dev)
+    fill(100)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            call(og, ws_g, st_g)
+    seen_residual = False
+    for seed in (101, 102, 103, 104):
+        fill(seed)
+        graph.replay()
+        call(oe, ws_e, st_e)
+        torch.cuda.synchronize()
+        assert int(st_g.item()) == 0 and int(st_e.item()) == 0
+        for k in og:
+            assert torch.equal(og[k], oe[k]), f"seed {seed}: {k}"
+        seen_residual |= bool((oe["next_mode"] == 0).any())
+    assert seen_residual

@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import speculative_verify_accept_step_b300 as lib
 from _gpu import assert_attention_close, gpu_attention, oracle_attention
 from speculative_verify_accept_step_b300 import workloads as wl
 
@@ -130,3 +131,39 @@ def test_bad_page_id_sets_status(cuda_device):
     a["page_table"][1, 1] = 10_000
     _, st = gpu_attention(a, R)
     assert st == 1
+
+
+def test_graph_replays_merge_split_units(cuda_device):
+    """A CUDA graph replays a launch with its parameters frozen, the merge
+    counters' epoch included: every replay must still merge the parts of a
+    unit the balanced split cut (the last part clears its counter)."""
+    w = wl.WORKLOADS["isd_c64_n4_ctx4096"]
+    a = wl.attention_inputs(w)
+    eager, st = gpu_attention(a, w.rows_full)
+    assert st == 0
+    dev = "cuda"
+    q = a["q"].to(dev)
+    T, Hq, D = q.shape
+    num_pages, Hkv, P, _ = a["k_cache"].shape
+    C = a["page_table"].shape[0]
+    dv = {k: a[k].to(dev) for k in ("k_new", "v_new", "k_cache", "v_cache", "page_table",
+                                    "seq_lens", "qo_indptr")}
+    ws = torch.empty(lib.idlm_isd_attention_workspace_size(C, Hq, Hkv, D, P, w.rows_full,
+                                                           lib.IDLM_BF16),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            lib.idlm_isd_attention(q, dv["k_new"], dv["v_new"], dv["k_cache"], dv["v_cache"],
+                                   dv["page_table"], dv["seq_lens"], dv["qo_indptr"], out, ws,
+                                   st, max_rows=w.rows_full, sm_scale=a["sm_scale"])
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(out, eager)

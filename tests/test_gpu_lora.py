@@ -245,3 +245,30 @@ def test_grouped_projections_match_the_separate_ones(cuda_device, r):
         ref = isd.gated_lora(f64(x), f64(ws_[i]), f64(as_[i]), f64(bs_[i]), g.numpy(), 1.0)
         assert_close(yg[:, n0:n0 + n], ref)
         n0 += n
+
+
+def test_graph_replays_sum_the_adapter_slices(cuda_device):
+    """Rank 16 at K = 4096 computes T = g s X A^T in several K slices, summed
+    by the last slice of each block to arrive; a CUDA graph replays the
+    launch with its epoch frozen, and every replay must still sum them."""
+    M, K, N, r = 448, 4096, 512, 16
+    x, w, a, b, g = case(M, K, N, r, seed=31)
+    eager = gpu_lora(x, w, a, b, g, 1.0)
+    dev = "cuda"
+    xs, ws_, as_, bs, gs = (t.to(dev) for t in (x, w, a, b, g))
+    ws = torch.empty(lib.idlm_gated_lora_workspace_size(M, K, N, r), dtype=torch.uint8,
+                     device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            lib.idlm_gated_lora(xs, ws_, as_, bs, gs, 1.0, y, ws, st)
+    for _ in range(3):
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(y, eager)
