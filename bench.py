@@ -43,9 +43,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-lora", action="store_true", help="skip the gated-LoRA leg")
+    ap.add_argument("--no-loop", action="store_true", help="skip the decode-loop leg")
     ap.add_argument("--no-ragged", action="store_true",
                     help="skip the ragged 1k-32k workload leg")
-    ap.add_argument("--leg", default="step", choices=["step", "lora", "layer"],
+    ap.add_argument("--leg", default="step", choices=["step", "lora", "layer", "loop"],
                     help="lora: only the gated-LoRA projections (prints their JSON)")
     ap.add_argument("--lora-reps", type=int, default=20)
     ap.add_argument("--lora-rank", type=int, default=None)
@@ -170,6 +171,55 @@ def layer_leg(dev, reps=10):
         torch.cuda.empty_cache()
     res["alpha_pages"] = 1.12
     return res
+
+
+def loop_leg(dev, steps=200, warm=10, target=0.9):
+    """The stationary-batch decode loop (f1) on the device: the headline batch
+    (64 requests, N = 4, V = 151936, 4096-token contexts, 32/8 heads of 128)
+    stepping through the synthetic model, attention, accept, commit and the
+    hand-off to the next step, `steps` steps replayed from one CUDA graph.
+    SAMPLE-mode proposals, so that the realised acceptance is the synthetic
+    model's overlap (target 0.9).  tokens_per_forward is the pages' TPF,
+    measured; the closed form is evaluated at the acceptance the loop
+    realised.  The synthetic model's kernel (which writes the step's logits,
+    standing in for the LM head) is inside the timed region."""
+    import json as _json
+    import speculative_verify_accept_step_b300 as L
+    from speculative_verify_accept_step_b300.loop import StationaryLoop
+    C, N, V = 64, 4, 151936
+
+    def tpf_closed_form(p, n):
+        # memory-bound tokens per forward of the speedup panel:
+        # (2 + p + ... + p^(n-2)) / (2 - p^(n-1))
+        return (2.0 + sum(p ** i for i in range(1, n - 1))) / (2.0 - p ** (n - 1))
+    path = os.path.join(ROOT, "speculative_verify_accept_step_b300", "synth_noise_table.json")
+    with open(path) as f:
+        sigma = float(_json.load(f)["sigma"][str(target)])
+    lp = StationaryLoop(C, N, V, torch.arange(C), torch.full((C,), 4096), [sigma] * C,
+                        steps=warm + steps + 1, seed=11, proposal_mode=L.PROPOSE_SAMPLE,
+                        attention=dict(Hq=32, Hkv=8, D=128), hist_cap=8, dev=dev)
+    lp.capture(warm).replay()
+    before = lp.results()
+    g = lp.capture(steps, step0=warm)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    after = lp.results()
+    assert after["status"] == 0, f"device status {after['status']}"
+    ms = e0.elapsed_time(e1)
+    d = {k: int((after[k] - before[k]).sum()) for k in ("tokens", "forwards", "accepted",
+                                                       "tested")}
+    p_hat = d["accepted"] / max(d["tested"], 1)
+    tpf = d["tokens"] / max(d["forwards"], 1)
+    return {"requests": C, "N": N, "context": 4096, "steps": steps, "graph": True,
+            "proposals": "sample", "target_acceptance": target,
+            "realised_acceptance": p_hat, "tokens_per_forward": tpf,
+            "tpf_closed_form_at_realised": tpf_closed_form(p_hat, N),
+            "ms_per_step": ms / steps, "tokens_per_s": d["tokens"] / (ms * 1e-3),
+            "launches_per_step": 5,
+            "note": "synthetic model kernel (logits for the step) inside the timed region"}
 
 
 def source_hash(name):
@@ -460,6 +510,12 @@ def run_ours(args):
             layer = layer_leg(dev)
         except Exception as e:   # reported, never fatal to the step's line
             layer = {"error": str(e)[:300]}
+    loop = None
+    if not args.profile_run and not args.no_loop:
+        try:
+            loop = loop_leg(dev)
+        except Exception as e:   # reported, never fatal to the step's line
+            loop = {"error": str(e)[:300]}
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.profile_run:
         cpu = cpu_baseline(w, st.host)
@@ -507,6 +563,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "lora": lora,
         "layer": layer,
+        "loop": loop,
         "workloads": {"isd_c64_n4_ctx1k_32k": ragged} if ragged else None,
     }
     print(json.dumps(line))
@@ -893,6 +950,10 @@ def main():
         build()
     if args.leg == "layer":
         print(json.dumps(layer_leg(torch.device("cuda", 0))))
+        return
+    if args.leg == "loop":
+        torch.cuda.set_device(0)
+        print(json.dumps(loop_leg(torch.device("cuda", 0))))
         return
     if args.leg == "lora":
         dev = torch.device("cuda", 0)

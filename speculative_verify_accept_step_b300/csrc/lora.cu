@@ -24,9 +24,13 @@
 // group of weight rows: a tile's adapter steps read its group's T columns.
 //
 // Kernels (three launches per slice of <= 448 token rows):
-//   lora_t_kernel      T = g s X A^T for every group (mma.sync, full K per
-//                      CTA, no cross-CTA sums), stored bf16 [M x groups*R64];
-//                      B padded to 64-value blocks where r % 64 != 0.
+//   lora_t_kernel      T = g s X A^T for every group (mma.sync), K split
+//                      over a few CTAs whose slices the last of them to
+//                      finish adds in slice order; stored bf16
+//                      [M x groups*R64]; B padded to 64-value blocks where
+//                      r % 64 != 0.  Where r % 64 == 0, T is instead one
+//                      more lora_gemm_kernel call (A as the weight, r = 0,
+//                      the gate and scale applied to its rows).
 //   lora_gemm_kernel   tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in
 //                      TMEM), operands staged by TMA (cp.async.bulk.tensor,
 //                      128-byte swizzle) in a ring of up to 8 stages.  Warp 0
