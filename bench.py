@@ -209,6 +209,17 @@ def loop_leg(dev, steps=200, warm=10, target=0.9):
     after = lp.results()
     assert after["status"] == 0, f"device status {after['status']}"
     ms = e0.elapsed_time(e1)
+    # the synthetic model alone, on the last step's layout (it stands in for
+    # the LM's forward pass and is not part of the ISD step)
+    reps = 20
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record()
+    for k in range(reps):
+        L.idlm_synth_logits(lp.logits[k % 2], lp.qo, lp.row_req, lp.row_pos, lp.row_token,
+                            lp.scale_z, lp.scale_e, 11, 10_000 + k)
+    e3.record()
+    torch.cuda.synchronize()
+    model_ms = e2.elapsed_time(e3) / reps
     d = {k: int((after[k] - before[k]).sum()) for k in ("tokens", "forwards", "accepted",
                                                        "tested")}
     p_hat = d["accepted"] / max(d["tested"], 1)
@@ -218,8 +229,11 @@ def loop_leg(dev, steps=200, warm=10, target=0.9):
             "realised_acceptance": p_hat, "tokens_per_forward": tpf,
             "tpf_closed_form_at_realised": tpf_closed_form(p_hat, N),
             "ms_per_step": ms / steps, "tokens_per_s": d["tokens"] / (ms * 1e-3),
+            "model_ms_per_step": model_ms,
+            "tokens_per_s_without_model": d["tokens"] / ((ms - model_ms * steps) * 1e-3),
             "launches_per_step": 5,
-            "note": "synthetic model kernel (logits for the step) inside the timed region"}
+            "note": "ms_per_step includes the synthetic model kernel (the step's logits, one "
+                    "Philox4x32-10 per logit); model_ms_per_step is that kernel timed alone"}
 
 
 def source_hash(name):
