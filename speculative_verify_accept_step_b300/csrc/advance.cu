@@ -12,10 +12,10 @@
 // cache) and d_k the MASK proposals of this step.  After a rejection it
 // continues FRESH: rows [anchor, MASK x (N-1)] at positions L .. L + N - 1.
 //
-// One kernel: every CTA scans the row counts of all requests (so that no CTA
-// waits for another), CTA 0 writes qo_indptr, and each CTA fills the rows of
-// its 64 requests (request, position, input token; -1 at MASK rows) and
-// advances their counters and token history.
+// One kernel: every CTA sums the row counts of the requests before its own
+// (so that no CTA waits for another), CTA 0 writes qo_indptr[0], and each CTA
+// fills the rows of its 256 requests (request, position, input token; -1 at
+// MASK rows) and advances their counters and token history.
 #include <algorithm>
 
 #include "common.cuh"
@@ -25,7 +25,8 @@ namespace idlm {
 namespace adv {
 
 constexpr int kThreads = 256;
-constexpr int kReqPerCta = 64;
+constexpr int kWarps = kThreads / 32;
+constexpr int kReqPerCta = kThreads;  // one thread per request in the scalar phase
 
 struct Params {
   int C, N, T;
@@ -52,63 +53,66 @@ __device__ __forceinline__ int rows_of(const Params& p, int c) {
   return p.next_mode[c] == IDLM_MODE_FULL ? 2 * p.N - 1 : p.N;
 }
 
+// Two phases per CTA of 256 requests.  Scalar phase: thread j owns request
+// c_lo + j and issues all of its loads (mode, emitted count, length) before
+// using any, so the CTA pays one memory latency where a serial walk over
+// the requests paid one per request; the rows before this CTA come from a
+// strided sum over the earlier requests' modes, the rows within it from a
+// shuffle scan.  Row phase: the CTA's (request, row) pairs are spread flat
+// over its threads, so consecutive threads write consecutive rows.
 __global__ void __launch_bounds__(kThreads) advance_kernel(const Params p) {
-  __shared__ int warp_sum[kThreads / 32];
-  __shared__ int cta_base;
+  __shared__ int warp_rows[kWarps];
+  __shared__ int warp_before[kWarps];
+  __shared__ int s_r0[kReqPerCta];
+  __shared__ int s_rows[kReqPerCta];  // 0 for a request whose inputs are out of range
+  __shared__ int s_ncl[kReqPerCta];
+  __shared__ int s_pos[kReqPerCta];
+  __shared__ int s_anchor[kReqPerCta];
+  __shared__ int s_used;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c_lo = blockIdx.x * kReqPerCta;
-  const int c_hi = min(p.C, c_lo + kReqPerCta);
-  // rows of requests [0, c_lo): every thread sums a strided share
+  const int n_here = min(p.C - c_lo, kReqPerCta);
+  const int c = c_lo + tid;
+  const bool mine = tid < n_here;
+  int nm = 0, no = 0, L = 0;
+  if (mine) {
+    nm = p.next_mode[c];
+    no = p.n_out[c];
+    L = p.seq_lens[c];
+  }
   int before = 0;
-  for (int c = tid; c < c_lo; c += kThreads) before += rows_of(p, c);
+#pragma unroll 4
+  for (int k = tid; k < c_lo; k += kThreads) before += rows_of(p, k);
+  const bool full = nm == IDLM_MODE_FULL;
+  const int rows = mine ? (full ? 2 * p.N - 1 : p.N) : 0;
+  int incl = rows;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
 #pragma unroll
   for (int o = 16; o; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
-  if (lane == 0) warp_sum[warp] = before;
+  if (lane == 31) warp_rows[warp] = incl;
+  if (lane == 0) warp_before[warp] = before;
   __syncthreads();
-  if (tid == 0) {
-    int s = 0;
-    for (int w = 0; w < kThreads / 32; ++w) s += warp_sum[w];
-    cta_base = s;
-  }
-  __syncthreads();
-  // exclusive scan of this CTA's requests (at most 64: two warps' worth)
-  __shared__ int first_row[kReqPerCta + 1];
-  if (tid == 0) {
-    int acc = cta_base;
-    for (int c = c_lo; c < c_hi; ++c) {
-      first_row[c - c_lo] = acc;
-      acc += rows_of(p, c);
-    }
-    first_row[c_hi - c_lo] = acc;
-  }
-  __syncthreads();
+  int r0 = incl - rows;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) r0 += warp_before[w] + (w < warp ? warp_rows[w] : 0);
   if (blockIdx.x == 0 && tid == 0) p.qo[0] = 0;
-  for (int c = c_lo + tid; c < c_hi; c += kThreads) p.qo[c + 1] = first_row[c - c_lo + 1];
-  // the rows of each request: one warp per request
-  const int M = p.N - 1;
-  for (int c = c_lo + warp; c < c_hi; c += kThreads / 32) {
-    const int r0 = first_row[c - c_lo];
-    const bool full = p.next_mode[c] == IDLM_MODE_FULL;
-    const int rows = full ? 2 * p.N - 1 : p.N;
-    const int ncl = full ? p.N : 1;
-    const int no = p.n_out[c];
-    const int L = p.seq_lens[c];
-    if (no < 1 || no > p.N || L < 0 || r0 + rows > p.T) {
-      if (lane == 0) set_status(p.status, IDLM_DEV_BAD_LAYOUT);
-      continue;
-    }
-    const int anchor = p.out_tokens[c * p.N + no - 1];
-    for (int r = lane; r < rows; r += 32) {
-      int tok;
-      if (r == 0) tok = anchor;
-      else if (r < ncl) tok = p.next_drafts[c * M + r - 1];
-      else tok = -1;
-      p.row_req[r0 + r] = c;
-      p.row_pos[r0 + r] = L + r;
-      p.row_token[r0 + r] = tok;
-    }
-    if (p.count && lane == 0) {
+  if (mine) {
+    p.qo[c + 1] = r0 + rows;
+    if (tid == n_here - 1) s_used = r0 + rows;
+    const bool bad = no < 1 || no > p.N || L < 0 || r0 + rows > p.T;
+    if (bad) set_status(p.status, IDLM_DEV_BAD_LAYOUT);
+    s_r0[tid] = r0;
+    s_rows[tid] = bad ? 0 : rows;
+    s_ncl[tid] = full ? p.N : 1;
+    s_pos[tid] = L;
+    s_anchor[tid] = bad ? 0 : p.out_tokens[c * p.N + no - 1];
+    if (!bad && p.count) {
       if (p.counters) {
+        const int M = p.N - 1;
         const int na = p.n_accepted ? p.n_accepted[c] : no - 1;
         const bool was_full = p.mode ? p.mode[c] == IDLM_MODE_FULL : false;
         p.counters[c] += no;
@@ -116,18 +120,32 @@ __global__ void __launch_bounds__(kThreads) advance_kernel(const Params p) {
         p.counters[2 * p.C + c] += na;
         p.counters[3 * p.C + c] += was_full ? min(na + 1, M) : 0;
       }
+      if (p.history) {
+        const int h = max(p.hist_len[c], 0);
+        int32_t* hist = p.history + static_cast<size_t>(c) * p.hist_cap;
+        for (int k = 0; k < no && h + k < p.hist_cap; ++k) hist[h + k] = p.out_tokens[c * p.N + k];
+        p.hist_len[c] = min(h + no, p.hist_cap);
+      }
     }
-    if (p.count && p.history && lane < no) {
-      const int at = p.hist_len[c] + lane;
-      if (at < p.hist_cap) p.history[static_cast<size_t>(c) * p.hist_cap + at] = p.out_tokens[c * p.N + lane];
-    }
-    __syncwarp();
-    if (p.count && p.history && lane == 0) p.hist_len[c] = min(p.hist_len[c] + no, p.hist_cap);
+  }
+  __syncthreads();
+  const int M = p.N - 1, R = 2 * p.N - 1;
+  for (int idx = tid; idx < n_here * R; idx += kThreads) {
+    const int j = idx / R, r = idx - j * R;
+    if (r >= s_rows[j]) continue;
+    const int cj = c_lo + j;
+    int tok;
+    if (r == 0) tok = s_anchor[j];
+    else if (r < s_ncl[j]) tok = p.next_drafts[cj * M + r - 1];
+    else tok = -1;
+    const int t = s_r0[j] + r;
+    p.row_req[t] = cj;
+    p.row_pos[t] = s_pos[j] + r;
+    p.row_token[t] = tok;
   }
   // rows past the last request: no request
   if (blockIdx.x == gridDim.x - 1) {
-    const int used = first_row[c_hi - c_lo];
-    for (int t = used + tid; t < p.T; t += kThreads) {
+    for (int t = s_used + tid; t < p.T; t += kThreads) {
       p.row_req[t] = 0;
       p.row_pos[t] = 0;
       p.row_token[t] = -2;

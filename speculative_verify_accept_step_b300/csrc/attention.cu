@@ -19,11 +19,14 @@
 // waiting) merges them.
 //
 // Per CTA: one producer warp issues TMA tile loads (cp.async.bulk.tensor,
-// 128-byte swizzle) of K and V pages into an 8-stage shared-memory ring
-// guarded by mbarriers; 2*MT consumer warps each own one m-tile and every
-// other block (two parity groups), compute S = Q K^T and O += P V with
+// 128-byte swizzle) into an 8-stage shared-memory ring guarded by mbarriers:
+// one 4 KB box per K page and one per V page, the two 64-column halves of D
+// being the box's outer dimension, with each page id read one block ahead.
+// 2*MT consumer warps each own one m-tile and every other pair of blocks (two
+// parity groups, 32 keys per step), compute S = Q K^T and O += P V with
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate) and an fp32 online softmax in
-// the log2 domain, and merge the two parity halves at the end of a unit.
+// the log2 domain, release a pair's first stage as soon as its V is read, and
+// merge the two parity halves at the end of a unit.
 //
 // The general path (fp32, or any other D / page size) is a plain kernel with
 // one warp per (row, head) walking the keys in order.
@@ -39,7 +42,14 @@ namespace attn {
 
 constexpr int D = 128;
 constexpr int PS = 16;
+// Ring depth, a multiple of 4: block i is consumed by parity group
+// (i >> 1) & 1 from stage i % STAGES, so a stage only ever serves one group,
+// whose warps wait on its phases in order, and a pair (i even) sits in two
+// stages of one phase.  With another depth a fast warp could wait on stage s
+// for block i while block i - STAGES (the other group's) has not landed, and
+// the parity test would pass on that older phase.
 constexpr int STAGES = 8;
+static_assert(STAGES % 4 == 0, "a stage must return to the parity group that read it");
 constexpr int BOX_BYTES = PS * 64 * 2;       // 16 rows x 128 bytes
 constexpr int STAGE_BYTES = 4 * BOX_BYTES;   // K lo/hi half, V lo/hi half
 constexpr int kMaxRequests = 8192;           // prefix array lives in shared memory
@@ -181,22 +191,20 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
       pref[c + 1] = (L + PS - 1) / PS + max(1, (R + PS - 1) / PS);   // temporarily the count
       sum += pref[c + 1];
     }
-    __syncthreads();
-    // serial scan of the per-thread sums by thread 0, then local fix-up
-    __shared__ int part[LY::kThreads + 1];
-    part[tid] = sum;
-    __syncthreads();
-    if (tid == 0) {
-      int acc = 0;
-      for (int t = 0; t < LY::kThreads; ++t) {
-        const int v = part[t];
-        part[t] = acc;
-        acc += v;
-      }
-      pref[0] = 0;
+    // exclusive scan of the per-thread sums: shuffles within a warp, then
+    // the warp totals
+    __shared__ int wsum[LY::kThreads / 32];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
+    if (lane == 31) wsum[warp] = incl;
+    if (tid == 0) pref[0] = 0;
     __syncthreads();
-    int acc = part[tid];
+    int acc = incl - sum;
+    for (int w = 0; w < warp; ++w) acc += wsum[w];
     for (int c = c0; c < c1; ++c) {
       acc += pref[c + 1];
       pref[c + 1] = acc;
@@ -219,14 +227,22 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
       prefetch_tensormap(&vn_map);
       Cursor cur = locate(p, pref, C, p.Hkv, lo);
       int issued = 0;
+      // the next block's page id is read while this block waits for its stage
+      auto page_of = [&](const Cursor& cc) {
+        return cc.k < cc.nbc ? p.page_table[static_cast<size_t>(cc.c) * p.max_pages + cc.k] : 0;
+      };
+      int page_nx = page_of(cur);
       for (long long j = lo; j < hi; ++j) {
+        const int page = page_nx;
+        Cursor nx = cur;
+        advance(nx, p, pref, C, p.Hkv);
+        if (j + 1 < hi) page_nx = page_of(nx);
         const int s = issued % STAGES;
         const uint32_t ph = (issued / STAGES) & 1;
         if (!mbar_wait_bounded(&empty[s], ph ^ 1, flags, p.status)) break;
         uint8_t* dst = stages + s * STAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
         if (cur.k < cur.nbc) {
-          const int page = p.page_table[static_cast<size_t>(cur.c) * p.max_pages + cur.k];
           int y;
           if (page < 0 || page >= p.num_pages) {
             set_status(p.status, IDLM_DEV_BAD_PAGE);
@@ -234,20 +250,16 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
           } else {
             y = (page * p.Hkv + cur.g) * PS;
           }
-          tma_load_2d(dst, &kc_map, &full[s], 0, y);
-          tma_load_2d(dst + BOX_BYTES, &kc_map, &full[s], 64, y);
-          tma_load_2d(dst + 2 * BOX_BYTES, &vc_map, &full[s], 0, y);
-          tma_load_2d(dst + 3 * BOX_BYTES, &vc_map, &full[s], 64, y);
+          tma_load_3d(dst, &kc_map, &full[s], 0, y, 0);
+          tma_load_3d(dst + 2 * BOX_BYTES, &vc_map, &full[s], 0, y, 0);
         } else {
           // new rows 16 b .. 16 b + 15 of the request (rows past T read zeros)
           const int t0 = p.qo_indptr[cur.c] + PS * (cur.k - cur.nbc);
-          tma_load_3d(dst, &kn_map, &full[s], 0, cur.g, t0);
-          tma_load_3d(dst + BOX_BYTES, &kn_map, &full[s], 64, cur.g, t0);
-          tma_load_3d(dst + 2 * BOX_BYTES, &vn_map, &full[s], 0, cur.g, t0);
-          tma_load_3d(dst + 3 * BOX_BYTES, &vn_map, &full[s], 64, cur.g, t0);
+          tma_load_4d(dst, &kn_map, &full[s], 0, cur.g, t0, 0);
+          tma_load_4d(dst + 2 * BOX_BYTES, &vn_map, &full[s], 0, cur.g, t0, 0);
         }
         ++issued;
-        advance(cur, p, pref, C, p.Hkv);
+        cur = nx;
       }
       // every issued copy must land before the CTA may exit
       for (int i = max(0, issued - STAGES); i < issued; ++i)
@@ -308,59 +320,91 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
 
-    for (; j < seg_end; ++j, ++i, advance(cur, p, pref, C, p.Hkv)) {
-      if ((i & 1) != par) continue;
-      const int s = i % STAGES;
+    // Blocks i and i + 1 (i even) go to parity group (i >> 1) & 1 together
+    // when both lie in this segment: 32 keys per step, four independent
+    // score chains and one max / rescale for both.  A block whose partner
+    // lies in another segment goes alone.
+    while (j < seg_end) {
+      const bool two = ((i & 1) == 0) && (j + 1 < seg_end);
+      const int nblk = two ? 2 : 1;
+      if (((i >> 1) & 1) != par) {
+        advance(cur, p, pref, C, p.Hkv);
+        if (two) advance(cur, p, pref, C, p.Hkv);
+        j += nblk;
+        i += nblk;
+        continue;
+      }
+      const int s0 = i % STAGES;
+      // a pair starts at an even stage, so both blocks share one ring phase
       const uint32_t ph = (i / STAGES) & 1;
-      const bool ok = mbar_wait_bounded(&full[s], ph, flags, p.status);
-      if (ok) {
-        const uint32_t kbase = smem_u32(stages + s * STAGE_BYTES);
-        const uint32_t vbase = kbase + 2 * BOX_BYTES;
-        // S = Q K^T
-        float sc[2][4];
+      const uint32_t kb0 = smem_u32(stages + s0 * STAGE_BYTES);
+      const uint32_t kb1 = kb0 + STAGE_BYTES;
+      // S = Q K^T: n-tiles 0, 1 are block i, n-tiles 2, 3 block i + 1; the
+      // second stage is awaited only once block i's chain is issued
+      float sc[4][4];
 #pragma unroll
-        for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+      for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+      auto scores = [&](uint32_t kb, float (&s0_)[4], float (&s1_)[4]) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const int ch = 2 * ks + kch_off;
-          const uint32_t addr = kbase + (ch >> 3) * BOX_BYTES + key_ld * 128 +
-                                (((ch & 7) ^ (key_ld & 7)) << 4);
+          const uint32_t off = (ch >> 3) * BOX_BYTES + key_ld * 128 +
+                               (((ch & 7) ^ (key_ld & 7)) << 4);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(addr, b0, b1, b2, b3);
-          mma_bf16_16816(sc[0], qa[ks], b0, b1);
-          mma_bf16_16816(sc[1], qa[ks], b2, b3);
+          ldsm_x4(kb + off, b0, b1, b2, b3);
+          mma_bf16_16816(s0_, qa[ks], b0, b1);
+          mma_bf16_16816(s1_, qa[ks], b2, b3);
         }
+      };
+      bool ok = mbar_wait_bounded(&full[s0], ph, flags, p.status);
+      if (ok) scores(kb0, sc[0], sc[1]);
+      if (two && ok) {
+        ok = mbar_wait_bounded(&full[s0 + 1], ph, flags, p.status);
+        if (ok) scores(kb1, sc[2], sc[3]);
+      }
+      bool released = false;
+      if (ok) {
         // mask keys past the request's context (cached pages) or past the
         // row's own position (the step's new rows, block b = k - nbc holds
         // rows 16 b ..); a full cached page needs no mask.  Column key =
-        // 8n + qc + e.
-        const int k = cur.k;
-        const bool full_page = k < nbc && (k + 1) * PS <= L;
-        if (!full_page) {
+        // 8n + qc + e within its block.
 #pragma unroll
-          for (int n = 0; n < 2; ++n) {
+        for (int bb = 0; bb < 2; ++bb) {
+          const int k = cur.k + bb;
+          if (bb == 1 && !two) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int key = 8 * n + qc + e;
-              bool ka, kb;
-              if (k < nbc) {
-                ka = kb = (k * PS + key) < L;
-              } else {
-                const int nr = PS * (k - nbc) + key;
-                ka = nr <= r_a;
-                kb = nr <= r_b;
+            for (int n = 2; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = kNegInf;
+            continue;
+          }
+          const bool full_page = k < nbc && (k + 1) * PS <= L;
+          if (!full_page) {
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int key = 8 * n + qc + e;
+                bool ka, kb;
+                if (k < nbc) {
+                  ka = kb = (k * PS + key) < L;
+                } else {
+                  const int nr = PS * (k - nbc) + key;
+                  ka = nr <= r_a;
+                  kb = nr <= r_b;
+                }
+                if (!ka) sc[2 * bb + n][e] = kNegInf;
+                if (!kb) sc[2 * bb + n][2 + e] = kNegInf;
               }
-              if (!ka) sc[n][e] = kNegInf;
-              if (!kb) sc[n][2 + e] = kNegInf;
             }
           }
         }
         // online softmax in the log2 domain: p = 2^(s * scale - m)
-        float mx_a = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-        float mx_b = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+        float mx_a = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])),
+                           fmaxf(fmaxf(sc[2][0], sc[2][1]), fmaxf(sc[3][0], sc[3][1])));
+        float mx_b = fmaxf(fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])),
+                           fmaxf(fmaxf(sc[2][2], sc[2][3]), fmaxf(sc[3][2], sc[3][3])));
         mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
         mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
         mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
         const float mn_a = fmaxf(m_a, mx_a * p.scale_log2), mn_b = fmaxf(m_b, mx_b * p.scale_log2);
         const float base_a = mn_a == kNegInf ? 0.f : mn_a;
@@ -380,34 +424,57 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
           m_a = mn_a;
           m_b = mn_b;
         }
-        float pr[2][4];
+        float pr[4][4];
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
+        for (int n = 0; n < 4; ++n) {
           pr[n][0] = fast_exp2(fmaf(sc[n][0], p.scale_log2, -base_a));
           pr[n][1] = fast_exp2(fmaf(sc[n][1], p.scale_log2, -base_a));
           pr[n][2] = fast_exp2(fmaf(sc[n][2], p.scale_log2, -base_b));
           pr[n][3] = fast_exp2(fmaf(sc[n][3], p.scale_log2, -base_b));
         }
-        l_a += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-        l_b += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-        uint32_t pa[4];
+        l_a += ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1])) +
+               ((pr[2][0] + pr[2][1]) + (pr[3][0] + pr[3][1]));
+        l_b += ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3])) +
+               ((pr[2][2] + pr[2][3]) + (pr[3][2] + pr[3][3]));
+        uint32_t pa[4], pb[4];
         pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
         pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
         pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
         pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+        pb[0] = pack_bf16x2(pr[2][0], pr[2][1]);
+        pb[1] = pack_bf16x2(pr[2][2], pr[2][3]);
+        pb[2] = pack_bf16x2(pr[3][0], pr[3][1]);
+        pb[3] = pack_bf16x2(pr[3][2], pr[3][3]);
+        // O += P V, block i (whose stage is then released) and block i + 1
+        auto pv = [&](uint32_t kb, const uint32_t (&pp)[4]) {
 #pragma unroll
-        for (int dp = 0; dp < 8; ++dp) {
-          const int ch = 2 * dp + vch_off;
-          const uint32_t addr = vbase + (ch >> 3) * BOX_BYTES + vkey * 128 +
-                                (((ch & 7) ^ (vkey & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(addr, b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * dp], pa, b0, b1);
-          mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+          for (int dp = 0; dp < 8; ++dp) {
+            const int ch = 2 * dp + vch_off;
+            const uint32_t off = 2 * BOX_BYTES + (ch >> 3) * BOX_BYTES + vkey * 128 +
+                                 (((ch & 7) ^ (vkey & 7)) << 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(kb + off, b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * dp], pp, b0, b1);
+            mma_bf16_16816(o[2 * dp + 1], pp, b2, b3);
+          }
+        };
+        pv(kb0, pa);
+        if (two) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s0]);
+          released = true;
+          pv(kb1, pb);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) {
+        if (!released) mbar_arrive(&empty[s0]);
+        if (two) mbar_arrive(&empty[s0 + 1]);
+      }
+      advance(cur, p, pref, C, p.Hkv);
+      if (two) advance(cur, p, pref, C, p.Hkv);
+      j += nblk;
+      i += nblk;
     }
 
     // ---- end of this unit's segment: merge the two parity halves
@@ -714,18 +781,19 @@ idlm_status launch_fast(const DeviceInfo& dev, const void* q, const void* k_new,
   p.scale_log2 = sm_scale * kLog2e;
 
   CUtensorMap kc, vc, kn, vn;
-  const uint64_t cdims[2] = {static_cast<uint64_t>(D),
-                             static_cast<uint64_t>(num_pages) * Hkv * PS};
-  const uint64_t cstr[1] = {D * 2};
-  const uint32_t cbox[2] = {64, PS};
-  const uint64_t ndims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
-                             static_cast<uint64_t>(T)};
-  const uint64_t nstr[2] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2};
-  const uint32_t nbox[3] = {64, 1, PS};
-  if (!encode_bf16_map(&kc, const_cast<void*>(k_cache), 2, cdims, cstr, cbox) ||
-      !encode_bf16_map(&vc, const_cast<void*>(v_cache), 2, cdims, cstr, cbox) ||
-      !encode_bf16_map(&kn, const_cast<void*>(k_new), 3, ndims, nstr, nbox) ||
-      !encode_bf16_map(&vn, const_cast<void*>(v_new), 3, ndims, nstr, nbox))
+  // Dimensions: 64 columns, rows, then the half of D (stride 128 bytes) as
+  // the outermost, so one box of a 16-row page lands as [half][row][64
+  // columns], 128-byte swizzled: the layout the consumers' ldmatrix reads.
+  const uint64_t cdims[3] = {64, static_cast<uint64_t>(num_pages) * Hkv * PS, 2};
+  const uint64_t cstr[2] = {D * 2, 128};
+  const uint32_t cbox[3] = {64, PS, 2};
+  const uint64_t ndims[4] = {64, static_cast<uint64_t>(Hkv), static_cast<uint64_t>(T), 2};
+  const uint64_t nstr[3] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2, 128};
+  const uint32_t nbox[4] = {64, 1, PS, 2};
+  if (!encode_bf16_map(&kc, const_cast<void*>(k_cache), 3, cdims, cstr, cbox) ||
+      !encode_bf16_map(&vc, const_cast<void*>(v_cache), 3, cdims, cstr, cbox) ||
+      !encode_bf16_map(&kn, const_cast<void*>(k_new), 4, ndims, nstr, nbox) ||
+      !encode_bf16_map(&vn, const_cast<void*>(v_new), 4, ndims, nstr, nbox))
     return IDLM_ERR_CUDA;
 
   paged_attn_kernel<MT><<<B, Layout<MT>::kThreads, Layout<MT>::bytes(C), stream>>>(kc, vc, kn, vn, p);

@@ -182,3 +182,71 @@ def test_tokens_per_forward_matches_the_closed_form(cuda_device, target, steps):
     assert abs(p_hat - target) < 0.01, f"realised acceptance {p_hat:.4f} vs target {target}"
     assert abs(tpf / closed_hat - 1) < 0.01, f"TPF {tpf:.4f} vs closed form {closed_hat:.4f}"
     assert abs(tpf / closed_target - 1) < 0.02, f"TPF {tpf:.4f} vs {closed_target:.4f}"
+
+
+@pytest.mark.parametrize("C,N", [(1, 2), (600, 4), (300, 16)])
+def test_advance_layout_over_several_ctas(cuda_device, C, N):
+    """The hand-off written request by request on the CPU from the row
+    layout of section "Inference & ISD": FULL rows [anchor, d_1 .. d_{N-1},
+    MASK x (N-1)], FRESH rows [anchor, MASK x (N-1)], at positions L, L+1,
+    ...; C = 600 spans three CTAs of requests and a ragged last one.  One
+    request with no emitted token is flagged and its rows left unwritten;
+    the history of a request that overflows hist_cap is cut at hist_cap."""
+    g = torch.Generator().manual_seed(C + N)
+    M = N - 1
+    mode = torch.randint(0, 2, (C,), generator=g, dtype=torch.uint8)
+    next_mode = torch.randint(0, 2, (C,), generator=g, dtype=torch.uint8)
+    n_out = torch.randint(1, N + 1, (C,), generator=g, dtype=torch.int32)
+    bad = C // 2 if C > 1 else -1
+    if bad >= 0:
+        n_out[bad] = 0
+    n_acc = (n_out - 1).clamp(min=0)
+    out_tokens = torch.randint(0, 1 << 20, (C, N), generator=g, dtype=torch.int32)
+    drafts = torch.randint(0, 1 << 20, (C, M), generator=g, dtype=torch.int32)
+    seq = torch.randint(0, 5000, (C,), generator=g, dtype=torch.int32)
+    rows = torch.tensor(isd.rows_per_request(next_mode.numpy(), N), dtype=torch.int64)
+    T = C * (2 * N - 1) + 5
+    cap = 6
+    hist_len = torch.randint(0, cap + 1, (C,), generator=g, dtype=torch.int32)
+    history = torch.randint(0, 9, (C, cap), generator=g, dtype=torch.int32)
+    counters = torch.randint(0, 50, (4, C), generator=g, dtype=torch.int32)
+    d = lambda x: x.to(cuda_device)
+    qo, rr, rp, rt = (torch.full((n,), -7, dtype=torch.int32, device=cuda_device)
+                      for n in (C + 1, T, T, T))
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    cnt_d, hist_d, hl_d = d(counters.clone()), d(history.clone()), d(hist_len.clone())
+    lib.idlm_isd_advance(N, d(mode), d(next_mode), d(out_tokens), d(n_out), d(n_acc), d(drafts),
+                         d(seq), qo, rr, rp, rt, status, counters=cnt_d, history=hist_d,
+                         hist_len=hl_d, count=True)
+    torch.cuda.synchronize()
+    want_qo = torch.zeros(C + 1, dtype=torch.int64)
+    want_qo[1:] = torch.cumsum(rows, 0)
+    assert torch.equal(qo.cpu().long(), want_qo)
+    assert int(status.item()) == (3 if bad >= 0 else 0)  # 3: bad layout
+    rr, rp, rt = rr.cpu(), rp.cpu(), rt.cpu()
+    cnt, hist, hl = cnt_d.cpu(), hist_d.cpu(), hl_d.cpu()
+    for c in range(C):
+        r0, n = int(want_qo[c]), int(rows[c])
+        if c == bad:
+            assert torch.all(rr[r0:r0 + n] == -7) and torch.equal(cnt[:, c], counters[:, c])
+            assert torch.equal(hist[c], history[c]) and int(hl[c]) == int(hist_len[c])
+            continue
+        no, ncl = int(n_out[c]), (N if int(next_mode[c]) == lib.MODE_FULL else 1)
+        want_tok = [int(out_tokens[c, no - 1])] + [int(drafts[c, k]) for k in range(ncl - 1)]
+        want_tok += [-1] * (n - ncl)
+        assert rr[r0:r0 + n].tolist() == [c] * n
+        assert rp[r0:r0 + n].tolist() == list(range(int(seq[c]), int(seq[c]) + n))
+        assert rt[r0:r0 + n].tolist() == want_tok, f"request {c}"
+        was_full = int(mode[c]) == lib.MODE_FULL
+        na = int(n_acc[c])
+        assert cnt[:, c].tolist() == [int(counters[0, c]) + no, int(counters[1, c]) + 1,
+                                      int(counters[2, c]) + na,
+                                      int(counters[3, c]) + (min(na + 1, M) if was_full else 0)]
+        h = int(hist_len[c])
+        want_h = history[c].clone()
+        for k in range(no):
+            if h + k < cap:
+                want_h[h + k] = out_tokens[c, k]
+        assert torch.equal(hist[c], want_h) and int(hl[c]) == min(h + no, cap)
+    used = int(want_qo[C])
+    assert torch.all(rr[used:] == 0) and torch.all(rp[used:] == 0) and torch.all(rt[used:] == -2)
