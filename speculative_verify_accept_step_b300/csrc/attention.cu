@@ -76,7 +76,7 @@ struct Layout {
   static constexpr int kThreads = 32 * (1 + kConsumers);
   static constexpr size_t kStageOff = 0;
   static constexpr size_t kMergeOOff = kStageOff + size_t(STAGES) * STAGE_BYTES;
-  static constexpr size_t kMergeMLOff = kMergeOOff + size_t(MT) * 16 * D * 4;
+  static constexpr size_t kMergeMLOff = kMergeOOff + size_t(16) * D * 4;   // one m-tile's O
   static constexpr size_t kBarOff = kMergeMLOff + size_t(MT) * 16 * 2 * 4;
   static constexpr size_t kFlagOff = kBarOff + 2 * STAGES * 8;
   static constexpr size_t kPrefOff = kFlagOff + 16;
@@ -482,44 +482,49 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-    float* mo = merge_o + mt * 16 * D;
+    // the m-tiles take turns through one O buffer (all consumer warps meet
+    // at named barrier 2 + MT); a smaller CTA footprint and fewer live
+    // values measured faster than one buffer per m-tile
+    float* mo = merge_o;
     float* mml = merge_ml + mt * 32;
-    if (par == 1) {
+    for (int r = 0; r < MT; ++r) {
+      if (mt == r && par == 1) {
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        *reinterpret_cast<float2*>(mo + qr * D + 8 * n + qc) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(mo + (qr + 8) * D + 8 * n + qc) = make_float2(o[n][2], o[n][3]);
+        for (int n = 0; n < 16; ++n) {
+          *reinterpret_cast<float2*>(mo + qr * D + 8 * n + qc) = make_float2(o[n][0], o[n][1]);
+          *reinterpret_cast<float2*>(mo + (qr + 8) * D + 8 * n + qc) = make_float2(o[n][2], o[n][3]);
+        }
+        if ((lane & 3) == 0) {
+          mml[2 * qr] = m_a;
+          mml[2 * qr + 1] = l_a;
+          mml[2 * (qr + 8)] = m_b;
+          mml[2 * (qr + 8) + 1] = l_b;
+        }
       }
-      if ((lane & 3) == 0) {
-        mml[2 * qr] = m_a;
-        mml[2 * qr + 1] = l_a;
-        mml[2 * (qr + 8)] = m_b;
-        mml[2 * (qr + 8) + 1] = l_b;
-      }
-    }
-    named_bar(1 + mt, 64);
-    if (par == 0) {
-      const float m2a = mml[2 * qr], l2a = mml[2 * qr + 1];
-      const float m2b = mml[2 * (qr + 8)], l2b = mml[2 * (qr + 8) + 1];
-      const float Ma = fmaxf(m_a, m2a), Mb = fmaxf(m_b, m2b);
-      const float ba = Ma == kNegInf ? 0.f : Ma, bb = Mb == kNegInf ? 0.f : Mb;
-      const float fa1 = fast_exp2(m_a - ba), fa2 = fast_exp2(m2a - ba);
-      const float fb1 = fast_exp2(m_b - bb), fb2 = fast_exp2(m2b - bb);
-      l_a = l_a * fa1 + l2a * fa2;
-      l_b = l_b * fb1 + l2b * fb2;
-      m_a = Ma;
-      m_b = Mb;
+      named_bar(2 + MT, 64 * MT);
+      if (mt == r && par == 0) {
+        const float m2a = mml[2 * qr], l2a = mml[2 * qr + 1];
+        const float m2b = mml[2 * (qr + 8)], l2b = mml[2 * (qr + 8) + 1];
+        const float Ma = fmaxf(m_a, m2a), Mb = fmaxf(m_b, m2b);
+        const float ba = Ma == kNegInf ? 0.f : Ma, bb = Mb == kNegInf ? 0.f : Mb;
+        const float fa1 = fast_exp2(m_a - ba), fa2 = fast_exp2(m2a - ba);
+        const float fb1 = fast_exp2(m_b - bb), fb2 = fast_exp2(m2b - bb);
+        l_a = l_a * fa1 + l2a * fa2;
+        l_b = l_b * fb1 + l2b * fb2;
+        m_a = Ma;
+        m_b = Mb;
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const float2 xa = *reinterpret_cast<const float2*>(mo + qr * D + 8 * n + qc);
-        const float2 xb = *reinterpret_cast<const float2*>(mo + (qr + 8) * D + 8 * n + qc);
-        o[n][0] = o[n][0] * fa1 + xa.x * fa2;
-        o[n][1] = o[n][1] * fa1 + xa.y * fa2;
-        o[n][2] = o[n][2] * fb1 + xb.x * fb2;
-        o[n][3] = o[n][3] * fb1 + xb.y * fb2;
+        for (int n = 0; n < 16; ++n) {
+          const float2 xa = *reinterpret_cast<const float2*>(mo + qr * D + 8 * n + qc);
+          const float2 xb = *reinterpret_cast<const float2*>(mo + (qr + 8) * D + 8 * n + qc);
+          o[n][0] = o[n][0] * fa1 + xa.x * fa2;
+          o[n][1] = o[n][1] * fa1 + xa.y * fa2;
+          o[n][2] = o[n][2] * fb1 + xb.x * fb2;
+          o[n][3] = o[n][3] * fb1 + xb.y * fb2;
+        }
       }
+      named_bar(2 + MT, 64 * MT);
     }
-    named_bar(1 + mt, 64);
 
     if (par == 0) {
       const int h_a = g * G + hl_a, h_b = g * G + hl_b;
