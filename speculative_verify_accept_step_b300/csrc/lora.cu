@@ -287,21 +287,23 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
 // ------------------------------------------------------------------ T = g s X A^T
 //
 // T [M x rt] (rt = groups * r adapter columns) is a small product with a
-// long K, so each CTA takes a block of 16 token rows x CB <= 64 columns and
-// one slice of K: it stages its X rows and A rows for the slice in shared
-// memory with 1-D bulk copies (every row in flight at once), then its 8
-// warps (one 8-column MMA tile each) run mma.sync m16n8k16 (bf16 in, fp32
-// accumulate) over the slice from shared memory.  Slices are summed in slice
-// order by the last CTA of the (rows, columns) block to finish (an arrival
-// counter tagged with the launch's epoch, so a fresh workspace needs no
-// clearing, and cleared by that last CTA, so a graph replay of the launch
-// finds it at zero).  T = g s (X A^T) is stored in bf16 at T64[m][group * R64 + j],
-// zeros at gated-off rows and in the padding columns j >= r.  Extra CTAs
-// copy B to 64-value blocks (zeros past r) where r % 64 != 0.
+// long K.  One cluster of `kslices` CTAs takes a block of 16 token rows x
+// CB <= 64 columns, each CTA one slice of K: it stages its X rows and A rows
+// for the slice in shared memory with 1-D bulk copies (every row in flight
+// at once; a slice longer than the staging buffer goes in pieces), then its
+// warps (one 8-column MMA tile each, two accumulators) run mma.sync
+// m16n8k16 (bf16 in, fp32 accumulate).  The cluster's first CTA sums the
+// slices' 16 x CB results in slice order, reading the others' shared memory
+// (distributed shared memory), and stores T = g s (X A^T) in bf16 at
+// T64[m][group * R64 + j], zeros at gated-off rows and in the padding
+// columns j >= r.  Nothing goes through global memory but the operands and
+// T, and no CTA waits on a counter.  Extra CTAs copy B to 64-value blocks
+// (zeros past r) where r % 64 != 0.
 constexpr int kTRows = 16;
 constexpr int kTThreads = 256;
-constexpr int kTWarps = kTThreads / 32;
 constexpr int kTMaxCols = 64;
+constexpr int kTMaxSlices = 8;             // portable cluster size
+constexpr size_t kTSmemMax = 200 * 1024;   // staging budget per CTA
 
 struct TParams {
   const __nv_bfloat16* x;
@@ -311,11 +313,9 @@ struct TParams {
   float scale;
   int M, K, N, r, ngroups, R64;
   int rt;                       // ngroups * r
-  int cb;                       // columns per CTA (multiple of 8, <= 64)
+  int cb;                       // columns per cluster (multiple of 8, <= 64)
   int col_blocks, row_blocks, kslices, kl;   // kl: K per slice (multiple of 16)
-  float* tpart;                 // [row_blocks * col_blocks][kslices][16][cb] fp32
-  unsigned long long* tcount;   // [row_blocks * col_blocks]: epoch << 32 | slices done
-  unsigned long long epoch;
+  int kc;                       // K staged at once (multiple of 16, <= kl)
   int32_t* status;
   __nv_bfloat16* t64;           // [M, ngroups * R64]
   __nv_bfloat16* b64;           // [N, R64]
@@ -330,11 +330,14 @@ __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r
 __global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
   extern __shared__ uint8_t tsm_raw[];
   __shared__ uint64_t bar;
-  __shared__ int last;
   __shared__ float red[kTRows][kTMaxCols];
+  // the GEMM after this kernel may be scheduled now: it waits for this grid
+  // to finish before it reads anything
+  griddep_launch_dependents();
   const int tblocks = p.row_blocks * p.col_blocks * p.kslices;
   if (static_cast<int>(blockIdx.x) >= tblocks) {
-    // B -> B64: row n, 64-value blocks, zeros past r
+    // B -> B64: row n, 64-value blocks, zeros past r (clusters of these CTAs
+    // hold no T block and meet at no cluster barrier)
     const int n = (blockIdx.x - tblocks) * kTThreads + threadIdx.x;
     if (n < p.N) {
       const uint4* src = reinterpret_cast<const uint4*>(p.b + static_cast<size_t>(n) * p.r);
@@ -344,109 +347,112 @@ __global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
     return;
   }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int blk = blockIdx.x / p.kslices, ks = blockIdx.x % p.kslices;
+  const int blk = static_cast<int>(cluster_id_x()), ks = static_cast<int>(cluster_ctarank());
   const int rb = blk / p.col_blocks, cbk = blk % p.col_blocks;
   const int m0 = rb * kTRows, j0 = cbk * p.cb;
-  const int k0 = ks * p.kl, kl = min(p.kl, p.K - k0);   // K % 8 == 0, kl % 8 == 0
-  const int kl16 = (kl + 15) / 16 * 16;
-  const int stride = (p.kl + 8) * 2;                    // bytes per staged row (16-byte pad)
+  const int k0 = ks * p.kl, kl = max(0, min(p.kl, p.K - k0));   // K % 8 == 0, kl % 8 == 0
+  const int stride = (p.kc + 8) * 2;                             // bytes per staged row
   uint8_t* xs = tsm_raw + ((16 - (smem_u32(tsm_raw) & 15)) & 15);
   uint8_t* as = xs + kTRows * stride;
   const int nrows = min(kTRows, p.M - m0);
   const int ncols = min(p.cb, p.rt - j0);
-  // zero what the copies do not cover: rows past M or rt, and the K tail
-  // of every row up to the next multiple of 16
-  for (int e = tid; e < (kTRows + p.cb) * ((p.kl + 8) / 8); e += kTThreads) {
-    const int row = e / ((p.kl + 8) / 8), c8 = (e % ((p.kl + 8) / 8)) * 8;
-    const bool real = row < kTRows ? row < nrows : (row - kTRows) < ncols;
-    if (!real || c8 >= kl)
-      *reinterpret_cast<uint4*>((row < kTRows ? xs + row * stride : as + (row - kTRows) * stride) +
-                                c8 * 2) = make_uint4(0, 0, 0, 0);
-  }
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_barrier_init();
   }
-  __syncthreads();
-  if (tid == 0) mbar_arrive_expect_tx(&bar, static_cast<uint32_t>((nrows + ncols) * kl * 2));
-  __syncthreads();
-  // one row per thread, every copy in flight at once
-  if (tid < nrows)
-    bulk_g2s(xs + tid * stride, p.x + static_cast<size_t>(m0 + tid) * p.K + k0, kl * 2, &bar);
-  else if (tid >= kTRows && tid - kTRows < ncols)
-    bulk_g2s(as + (tid - kTRows) * stride, p.a + static_cast<size_t>(j0 + tid - kTRows) * p.K + k0,
-             kl * 2, &bar);
-  const bool ok = mbar_wait_bounded(&bar, 0, nullptr, p.status);
-  // warp w: output columns j0 + 8w .. 8w + 7
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (ok && warp * 8 < ncols) {
-    const uint32_t xb = smem_u32(xs), ab = smem_u32(as + warp * 8 * stride);
-    const int xr = lane & 15, xc = (lane >> 4) * 8;       // x4: rows 0-15, k 0-7 / 8-15
-    const int ar = lane & 7, ac = ((lane >> 3) & 1) * 8;  // x2: rows 0-7, k 0-7 / 8-15
-    for (int k = 0; k < kl16; k += 16) {
-      uint32_t a4[4], b0, b1;
-      ldsm_x4(xb + xr * stride + (k + xc) * 2, a4[0], a4[1], a4[2], a4[3]);
-      ldsm_x2(ab + ar * stride + (k + ac) * 2, b0, b1);
-      mma_bf16_16816(acc, a4, b0, b1);
+  // warp w: output columns j0 + 8w .. 8w + 7; four accumulators shorten the
+  // MMA dependency chain
+  float acc[4][4] = {};
+  const int xr = lane & 15, xc = (lane >> 4) * 8;       // x4: rows 0-15, k 0-7 / 8-15
+  const int ar = lane & 7, ac = ((lane >> 3) & 1) * 8;  // x2: rows 0-7, k 0-7 / 8-15
+  const int npieces = (kl + p.kc - 1) / p.kc;
+  for (int pc = 0; pc < npieces; ++pc) {
+    const int c0 = pc * p.kc, cl = min(p.kc, kl - c0);   // cl % 8 == 0
+    const int cl16 = (cl + 15) / 16 * 16;
+    __syncthreads();   // the barrier's init, and the MMAs of the piece before are done
+    // zeros where the MMAs read past the copies: whole rows past M or rt,
+    // and the last 8 values of a piece whose length is not a multiple of 16
+    const int zrows = (kTRows - nrows) + (p.cb - ncols);
+    for (int e = tid; e < zrows * (cl16 / 8); e += kTThreads) {
+      const int q = e / (cl16 / 8), c8 = (e % (cl16 / 8)) * 8;
+      uint8_t* row = q < kTRows - nrows ? xs + (nrows + q) * stride
+                                        : as + (ncols + q - (kTRows - nrows)) * stride;
+      *reinterpret_cast<uint4*>(row + c8 * 2) = make_uint4(0, 0, 0, 0);
+    }
+    if (cl < cl16) {
+      for (int i = tid; i < nrows + ncols; i += kTThreads) {
+        uint8_t* row = i < nrows ? xs + i * stride : as + (i - nrows) * stride;
+        *reinterpret_cast<uint4*>(row + cl * 2) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (tid == 0) mbar_arrive_expect_tx(&bar, static_cast<uint32_t>((nrows + ncols) * cl * 2));
+    __syncthreads();
+    // one row per thread, every copy in flight at once
+    if (tid < nrows)
+      bulk_g2s(xs + tid * stride, p.x + static_cast<size_t>(m0 + tid) * p.K + k0 + c0, cl * 2, &bar);
+    else if (tid >= kTRows && tid - kTRows < ncols)
+      bulk_g2s(as + (tid - kTRows) * stride,
+               p.a + static_cast<size_t>(j0 + tid - kTRows) * p.K + k0 + c0, cl * 2, &bar);
+    const bool ok = mbar_wait_bounded(&bar, pc & 1, nullptr, p.status);
+    if (ok && warp * 8 < ncols) {
+      const uint32_t xb = smem_u32(xs), ab = smem_u32(as + warp * 8 * stride);
+      int k = 0;
+      for (; k + 64 <= cl16; k += 64) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t a4[4], b0, b1;
+          ldsm_x4(xb + xr * stride + (k + 16 * u + xc) * 2, a4[0], a4[1], a4[2], a4[3]);
+          ldsm_x2(ab + ar * stride + (k + 16 * u + ac) * 2, b0, b1);
+          mma_bf16_16816(acc[u], a4, b0, b1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        if (k + 16 * u < cl16) {
+          uint32_t a4[4], b0, b1;
+          ldsm_x4(xb + xr * stride + (k + 16 * u + xc) * 2, a4[0], a4[1], a4[2], a4[3]);
+          ldsm_x2(ab + ar * stride + (k + 16 * u + ac) * 2, b0, b1);
+          mma_bf16_16816(acc[u], a4, b0, b1);
+        }
+      }
     }
   }
   // acc: rows g and g + 8, columns 2 t4, 2 t4 + 1 of the warp's 8
   const int g = lane >> 2, t4 = lane & 3;
-  const size_t tile = static_cast<size_t>(kTRows) * p.cb;
-  float* mine = p.tpart + (static_cast<size_t>(blk) * p.kslices + ks) * tile;
   if (warp * 8 < p.cb) {
     const int c = warp * 8 + 2 * t4;
-    if (p.kslices == 1) {
-      red[g][c] = acc[0];
-      red[g][c + 1] = acc[1];
-      red[g + 8][c] = acc[2];
-      red[g + 8][c + 1] = acc[3];
-    } else {
-      __stcg(mine + g * p.cb + c, acc[0]);
-      __stcg(mine + g * p.cb + c + 1, acc[1]);
-      __stcg(mine + (g + 8) * p.cb + c, acc[2]);
-      __stcg(mine + (g + 8) * p.cb + c + 1, acc[3]);
-    }
+    red[g][c] = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
+    red[g][c + 1] = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
+    red[g + 8][c] = (acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2]);
+    red[g + 8][c + 1] = (acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]);
   }
-  if (p.kslices > 1) {
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const unsigned long long tag = (p.epoch & 0xffffffffull) << 32;
-      unsigned long long* cnt = p.tcount + blk;
-      unsigned long long seen, old = *reinterpret_cast<volatile unsigned long long*>(cnt);
-      do {
-        seen = old;
-        const unsigned long long nv = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
-        old = atomicCAS(cnt, seen, nv);
-      } while (old != seen);
-      const unsigned long long now = ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
-      last = (now & 0xffffffffull) == static_cast<unsigned long long>(p.kslices);
-      // the last slice clears the counter: a CUDA graph replays this launch
-      // with the same epoch, and must find the count at zero again
-      if (last) atomicExch(cnt, 0ull);
-      __threadfence();
-    }
-    __syncthreads();
-    if (!last) return;
-    // the slices in slice order
-    const float* base = p.tpart + static_cast<size_t>(blk) * p.kslices * tile;
-    for (int e = tid; e < kTRows * p.cb; e += kTThreads) {
-      float v = 0.f;
-      for (int q = 0; q < p.kslices; ++q) v += __ldcg(base + q * tile + e);
-      red[e / p.cb][e % p.cb] = v;
-    }
-  }
-  __syncthreads();
+  // every slice's result is in its CTA's shared memory; each CTA of the
+  // cluster adds up a share of the block's elements over the slices, in
+  // slice order (all of an element's remote loads issued before the adds),
+  // and stores them as T
+  cluster_sync_all();
+  const int nel = kTRows * p.cb;
+  const int per = (nel + p.kslices - 1) / p.kslices;
+  const int e0 = ks * per, e1 = min(nel, e0 + per);
   const size_t tstride = static_cast<size_t>(p.ngroups) * p.R64;
-  for (int e = tid; e < kTRows * p.cb; e += kTThreads) {
+  for (int e = e0 + tid; e < e1; e += kTThreads) {
     const int i = e / p.cb, cl = e % p.cb;
+    const uint32_t addr = smem_u32(&red[i][cl]);
+    float part[kTMaxSlices];
+#pragma unroll
+    for (int q = 0; q < kTMaxSlices; ++q) part[q] = q < p.kslices ? ld_cluster_f32(addr, q) : 0.f;
+    float v = part[0];
+#pragma unroll
+    for (int q = 1; q < kTMaxSlices; ++q) v += part[q];
     const int m = m0 + i, col = j0 + cl;
     if (m >= p.M || col >= p.rt) continue;
-    const float v = p.gate[m] ? red[i][cl] * p.scale : 0.f;
+    const float tv = p.gate[m] ? v * p.scale : 0.f;
     const int grp = col / p.r, jj = col % p.r;
-    p.t64[static_cast<size_t>(m) * tstride + grp * p.R64 + jj] = __float2bfloat16_rn(v);
+    p.t64[static_cast<size_t>(m) * tstride + grp * p.R64 + jj] = __float2bfloat16_rn(tv);
   }
+  // the other CTAs' shared memory stays until every share is read
+  cluster_sync_all();
+  if (ks != 0) return;
   // zeros in the padding columns of every group whose last real column this
   // block holds
   const int pad = p.R64 - p.r;
@@ -462,22 +468,21 @@ __global__ void __launch_bounds__(kTThreads) lora_t_kernel(const TParams p) {
   }
 }
 
-// The adapter kernel's split of T over CTAs: CB columns per CTA, K slices so
-// that about one CTA per SM works and a CTA's staged rows fit in shared
-// memory.  Returns the dynamic shared memory per CTA.
+// The adapter kernel's split of T: CB columns per cluster, K slices (the
+// cluster's size, at most 8) so that about one CTA per SM works, and the
+// K staged at once so that a CTA's rows fit in shared memory.  Returns the
+// dynamic shared memory per CTA.
 inline size_t t_plan(int M, int K, int rt, int sms, int& cb, int& col_blocks, int& row_blocks,
-                     int& kslices, int& kl) {
+                     int& kslices, int& kl, int& kc) {
   col_blocks = (rt + kTMaxCols - 1) / kTMaxCols;
   cb = ((rt + col_blocks - 1) / col_blocks + 7) / 8 * 8;
   row_blocks = (M + kTRows - 1) / kTRows;
   const int base = row_blocks * col_blocks;
-  kslices = std::max(1, std::min(sms / base, (K + 255) / 256));
-  for (;;) {
-    kl = ((K + kslices - 1) / kslices + 15) / 16 * 16;
-    const size_t smem = 16 + static_cast<size_t>(kTRows + cb) * (kl + 8) * 2;
-    if (smem <= 160 * 1024 || kl <= 256) return smem;
-    ++kslices;
-  }
+  kslices = std::max(1, std::min(std::min(sms / base, kTMaxSlices), (K + 255) / 256));
+  kl = ((K + kslices - 1) / kslices + 15) / 16 * 16;
+  const int fit = static_cast<int>((kTSmemMax - 16) / (static_cast<size_t>(kTRows + cb) * 2)) - 8;
+  kc = std::max(16, std::min(kl, fit / 16 * 16));
+  return 16 + static_cast<size_t>(kTRows + cb) * (kc + 8) * 2;
 }
 
 // ------------------------------------------------------------ the GEMM
@@ -853,21 +858,17 @@ int max_grid() {
 int r64_of(int r) { return (r + lora::kPadW - 1) / lora::kPadW * lora::kPadW; }
 
 struct WsLayout {
-  size_t t64, b64, tpart, tcount, part, total;
+  size_t t64, b64, part, total;
 };
 WsLayout ws_layout(int M, int K, int N, int r, int ngroups) {
   const int Ms = std::min(M, lora::kMaxTokens);
   const size_t m16 = (Ms + 15) / 16 * 16;
   const size_t G = max_grid();
   const size_t R64 = r64_of(r);
-  int cb = 8, cbl = 1, rbl = 1, ks = 1, kl = 16;
-  if (r > 0) lora::t_plan(Ms, K, ngroups * r, static_cast<int>(G), cb, cbl, rbl, ks, kl);
   WsLayout l;
   l.t64 = 0;
   l.b64 = align_up(static_cast<size_t>(Ms) * ngroups * R64 * 2, 256);
-  l.tpart = l.b64 + align_up(static_cast<size_t>(N) * R64 * 2, 256);
-  l.tcount = l.tpart + align_up(static_cast<size_t>(rbl) * cbl * ks * lora::kTRows * cb * 4, 256);
-  l.part = l.tcount + align_up(static_cast<size_t>(rbl) * cbl * 8, 256);
+  l.part = l.b64 + align_up(static_cast<size_t>(N) * R64 * 2, 256);
   l.total = l.part + G * 2 * lora::kTileN * m16 * sizeof(float);
   return l;
 }
@@ -1086,7 +1087,7 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
       if (cudaFuncSetAttribute(lora::lora_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dev.max_smem_optin) != cudaSuccess ||
           cudaFuncSetAttribute(lora::lora_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               200 * 1024) != cudaSuccess)
+                               static_cast<int>(lora::kTSmemMax)) != cudaSuccess)
         return IDLM_ERR_CUDA;
       done[dev.device] = ctx;
     }
@@ -1161,11 +1162,6 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
       const idlm_status trc = launch_gemm(ta, tpl, stages, smem, status, stream);
       if (trc != IDLM_OK) return trc;
     } else if (r > 0) {
-      // launches get distinct epochs, so a fresh workspace needs no clearing;
-      // the last slice of a block clears its counter for graph replays
-      static std::atomic<unsigned long long> epoch_counter{
-          0x9e3779b97f4a7c15ull ^
-          static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};
       lora::TParams tp;
       tp.x = xs;
       tp.a = static_cast<const __nv_bfloat16*>(lora_a);
@@ -1180,16 +1176,28 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
       tp.R64 = R64;
       tp.rt = ngroups * r;
       const size_t tsmem = lora::t_plan(Ms, K, tp.rt, grid_cap, tp.cb, tp.col_blocks,
-                                        tp.row_blocks, tp.kslices, tp.kl);
-      tp.tpart = reinterpret_cast<float*>(wsb + wl.tpart);
-      tp.tcount = reinterpret_cast<unsigned long long*>(wsb + wl.tcount);
-      tp.epoch = ++epoch_counter;
+                                        tp.row_blocks, tp.kslices, tp.kl, tp.kc);
       tp.status = status;
       tp.t64 = t;
       tp.b64 = b64;
+      // one cluster of kslices CTAs per block of T; the B-copy CTAs after
+      // them fill whole clusters of their own
       const int tblocks = tp.row_blocks * tp.col_blocks * tp.kslices;
-      const int bblocks = pad_b ? (N + lora::kTThreads - 1) / lora::kTThreads : 0;
-      lora::lora_t_kernel<<<tblocks + bblocks, lora::kTThreads, tsmem, stream>>>(tp);
+      int bblocks = pad_b ? (N + lora::kTThreads - 1) / lora::kTThreads : 0;
+      bblocks = (bblocks + tp.kslices - 1) / tp.kslices * tp.kslices;
+      cudaLaunchAttribute tat[1];
+      tat[0].id = cudaLaunchAttributeClusterDimension;
+      tat[0].val.clusterDim.x = static_cast<unsigned>(tp.kslices);
+      tat[0].val.clusterDim.y = 1;
+      tat[0].val.clusterDim.z = 1;
+      cudaLaunchConfig_t tc = {};
+      tc.gridDim = dim3(tblocks + bblocks);
+      tc.blockDim = dim3(lora::kTThreads);
+      tc.dynamicSmemBytes = tsmem;
+      tc.stream = stream;
+      tc.attrs = tat;
+      tc.numAttrs = 1;
+      if (cudaLaunchKernelEx(&tc, lora::lora_t_kernel, tp) != cudaSuccess) return IDLM_ERR_CUDA;
       if (cudaGetLastError() != cudaSuccess) return IDLM_ERR_CUDA;
     }
 
