@@ -74,6 +74,21 @@ def test_more_than_16_rows_per_request(cuda_device, Hq, N):
     assert_attention_close(out, oracle_attention(a))
 
 
+@pytest.mark.parametrize("N", [2, 4, 8])
+def test_many_short_units_per_cta(cuda_device, N):
+    """300 requests with contexts of 0-160 tokens: every CTA of the grid walks
+    several short units, so the consumers' pairs of blocks meet unit
+    boundaries at both parities (a pair never spans two units: the block
+    before a boundary goes alone) and segments start on odd blocks; one to
+    four m-tiles (G (2N - 1) = 12, 28, 60 rows).  Every output is compared."""
+    rng = np.random.default_rng(N)
+    lens = [int(v) for v in rng.integers(0, 161, 300)]
+    a, R = _custom(len(lens), N, lens, seed=40 + N, fresh=tuple(range(0, 300, 7)))
+    out, st = gpu_attention(a, R)
+    assert st == 0
+    assert_attention_close(out, oracle_attention(a))
+
+
 def test_mixed_fresh_and_full_rows(cuda_device):
     lens = [40, 0, 300, 16]
     a, R = _custom(4, 4, lens, seed=11, fresh=(1, 2))
