@@ -264,6 +264,44 @@ idlm_status idlm_isd_accept(
     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Fused LM head + accept ([IDLM] "Inference & ISD": p and q both come from
+ * the one forward pass, whose last product is the LM head).
+ *
+ * logits = hidden W^T, then the accept step of idlm_isd_accept on them, in
+ * one call.  The GEMM (tcgen05, the gated-LoRA GEMM without an adapter)
+ * writes the logits once and, in the same epilogue, the softmax statistics
+ * of every logits row per 128-entry tile of the vocabulary, taken from the
+ * bf16 values it stores; a merge kernel turns them into the accept's
+ * per-chunk records and the accept runs without its own pass over the
+ * logits.  The draws (one chunk per inverse-CDF search, the two rows of a
+ * rejected draft's residual) read the logits written here.
+ *
+ *   hidden   [T, H] bf16, 16-byte aligned: the step's rows (the final hidden
+ *            states after the model's last norm)
+ *   w_vocab  [V, H] bf16, 16-byte aligned: the LM head's weights
+ *   logits   [T, V] bf16 out (16-byte aligned), the same logits that
+ *            idlm_isd_accept would take
+ *   the remaining arguments as for idlm_isd_accept with dtype = IDLM_BF16;
+ *   prev_logits is the previous step's `logits` buffer.
+ * Requirements: H % 8 == 0, V % 8 == 0, 2 <= N <= 16, temperature >= 0.
+ * Launches: the GEMM and (where its plan splits tiles) its fix-up, the merge
+ * kernel, then the accept's three kernels.  Workspace contents need no
+ * initialisation.
+ * ---------------------------------------------------------------------- */
+size_t idlm_lm_head_accept_workspace_size(int C, int T, int N, int H, int V);
+
+idlm_status idlm_lm_head_accept(
+    const void* hidden, const void* w_vocab, int H, void* logits, int V,
+    const int32_t* qo_indptr, const uint8_t* mode, const int32_t* drafts,
+    const float* draft_q_stats, const void* prev_logits, int prev_rows,
+    const int32_t* prev_mask_row0, int C, int T, int N, float temperature,
+    int proposal_mode, uint64_t seed, uint64_t step,
+    int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out, int32_t* n_commit,
+    int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+    int32_t* next_mask_row0, float* row_stats, float* dbg,
+    void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * Allocation-free accept.  The pages have no counterpart: this entry point
  * exists for callers that cannot allocate device memory -- a plugin whose
  * host owns all GPU memory and offers no scratch, or a decode loop held to a

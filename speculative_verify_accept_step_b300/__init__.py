@@ -11,4 +11,5 @@ from ._lib import (  # noqa: F401,E402
     idlm_gated_lora_grouped_workspace_size, idlm_isd_accept, idlm_isd_accept_noalloc,
     idlm_isd_accept_workspace_size, idlm_isd_attention, idlm_isd_attention_workspace_size,
     idlm_kv_commit, idlm_synth_logits, idlm_isd_advance, idlm_risd_layer,
-    idlm_risd_layer_workspace_size, layer_weights, lib, version)
+    idlm_risd_layer_workspace_size, idlm_lm_head_accept, idlm_lm_head_accept_workspace_size,
+    layer_weights, lib, version)

@@ -66,6 +66,13 @@ def lib():
             [vp, i32, i32] + [vp] * 5 + [i32, vp] + [i32, i32, i32, f32, i32, u64, u64]
             + [vp] * 10
             + [vp, sz, vp, vp])
+        L.idlm_lm_head_accept_workspace_size.restype = sz
+        L.idlm_lm_head_accept_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.idlm_lm_head_accept.restype = i32
+        L.idlm_lm_head_accept.argtypes = (
+            [vp, vp, i32, vp, i32] + [vp] * 4 + [vp, i32, vp] + [i32, i32, i32, f32, i32, u64, u64]
+            + [vp] * 10
+            + [vp, sz, vp, vp])
         L.idlm_isd_accept_noalloc.restype = i32
         L.idlm_isd_accept_noalloc.argtypes = (
             [vp, i32, i32] + [vp] * 5 + [i32, vp] + [i32, i32, i32, f32, i32, u64, u64]
@@ -175,6 +182,35 @@ def idlm_isd_accept(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits,
         _ptr(next_mode), _ptr(next_mask_row0), _ptr(row_stats), _ptr(dbg), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
     _check(rc, "idlm_isd_accept")
+
+
+def idlm_lm_head_accept_workspace_size(C, T, N, H, V):
+    return lib().idlm_lm_head_accept_workspace_size(C, T, N, H, V)
+
+
+def idlm_lm_head_accept(hidden, w_vocab, logits, qo_indptr, mode, drafts, draft_q_stats,
+                        prev_logits, prev_mask_row0, N, temperature, proposal_mode, seed, step,
+                        n_accepted, out_tokens, n_out, n_commit, next_drafts, next_q_stats,
+                        next_mode, next_mask_row0, workspace, status, row_stats=None, dbg=None,
+                        stream=None):
+    """logits = hidden @ w_vocab^T (written to `logits`, bf16 [T, V]), then the
+    accept step on them, with the vocabulary statistics taken in the GEMM's
+    epilogue instead of a separate pass over the logits."""
+    _contig(hidden, w_vocab, logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits,
+            prev_mask_row0, n_accepted, out_tokens, n_out, n_commit, next_drafts, next_q_stats,
+            next_mode, next_mask_row0, workspace, row_stats, dbg)
+    T, H = hidden.shape
+    V = w_vocab.shape[0]
+    C = mode.shape[0]
+    rc = lib().idlm_lm_head_accept(
+        _ptr(hidden), _ptr(w_vocab), H, _ptr(logits), V, _ptr(qo_indptr), _ptr(mode),
+        _ptr(drafts), _ptr(draft_q_stats), _ptr(prev_logits), prev_logits.shape[0],
+        _ptr(prev_mask_row0), C, T, N, float(temperature), int(proposal_mode), int(seed),
+        int(step), _ptr(n_accepted), _ptr(out_tokens), _ptr(n_out), _ptr(n_commit),
+        _ptr(next_drafts), _ptr(next_q_stats), _ptr(next_mode), _ptr(next_mask_row0),
+        _ptr(row_stats), _ptr(dbg), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _check(rc, "idlm_lm_head_accept")
 
 
 def idlm_isd_accept_noalloc(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits,

@@ -127,6 +127,8 @@ struct Params {
   uint64_t seed, step;
   int V, C, T, N, CH, nslice, chunk, greedy, propose, prev_rows;
   float s2;           // log2(e) / T
+  int part_given;     // 1: `part` already holds every chunk record (the fused LM head
+                      // wrote them); kernel 1 then only gathers the requests' inputs
 };
 
 template <typename T>
@@ -423,7 +425,7 @@ __global__ void __launch_bounds__(kK1Threads, 1) vocab_stream_kernel(const Param
   // rows in use: qo_indptr[C] (T is the capacity of the logits buffer, so a
   // fixed-shape loop can pass its largest row count every step)
   const int T_used = min(max(__ldg(p.qo + p.C), 0), p.T);
-  const long long W = static_cast<long long>(T_used) * p.CH;
+  const long long W = p.part_given ? 0 : static_cast<long long>(T_used) * p.CH;
   const long long lo = W * blockIdx.x / gridDim.x;
   const long long hi = W * (blockIdx.x + 1) / gridDim.x;
   const int n = static_cast<int>(hi - lo);
@@ -1012,6 +1014,46 @@ __global__ void __launch_bounds__(kWThreads) work_kernel(const Params p) {
   }
 }
 
+// Chunk records from the fused LM head's tile records: the tiles of 128
+// vocabulary entries that make up each 4096-entry chunk (bf16), merged in one
+// warp per (row, chunk): max of the maxima, the sums rescaled to it, the
+// largest value with the lowest index.
+constexpr int kLmTile = 128;
+__global__ void __launch_bounds__(256) lm_combine_kernel(const Partial* ts, int tiles, Partial* part,
+                                                        int rows, int CH, int greedy) {
+  const int w = static_cast<int>((blockIdx.x * 256u + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (w >= rows * CH) return;   // whole warps
+  const int row = w / CH, ch = w % CH;
+  constexpr int per = kItemBytes / 2 / kLmTile;   // tiles per chunk
+  static_assert(per == 32, "one lane per tile of a chunk");
+  const int tile = ch * per + lane;
+  Partial t;
+  t.m = kNegInf;
+  t.s = 0.f;
+  t.amax = kNegInf;
+  t.aidx = 0x7fffffff;
+  if (tile < tiles) t = ts[static_cast<size_t>(row) * tiles + tile];
+  float M = t.m;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float S = (greedy || t.m == kNegInf) ? 0.f : t.s * fast_exp2(t.m - M);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  float BX = t.amax;
+  int BI = t.aidx;
+#pragma unroll
+  for (int o = 16; o; o >>= 1)
+    argmax_merge(BX, BI, __shfl_xor_sync(0xffffffffu, BX, o), __shfl_xor_sync(0xffffffffu, BI, o));
+  if (lane == 0) {
+    Partial r;
+    r.m = greedy ? BX : M;
+    r.s = greedy ? 1.f : S;
+    r.amax = BX;
+    r.aidx = BI;
+    part[static_cast<size_t>(row) * CH + ch] = r;
+  }
+}
+
 inline int chunk_elems(int dtype) { return dtype == IDLM_BF16 ? kItemBytes / 2 : kItemBytes / 4; }
 inline int chunks_for(int V, int dtype) { return (V + chunk_elems(dtype) - 1) / chunk_elems(dtype); }
 
@@ -1105,15 +1147,19 @@ extern "C" size_t idlm_isd_accept_workspace_size(int C, int T, int N, int V) {
   return acc::workspace_bytes(C, T, V, IDLM_F32, nullptr, nullptr);
 }
 
-extern "C" idlm_status idlm_isd_accept(
-    const void* logits, int dtype, int V, const int32_t* qo_indptr, const uint8_t* mode,
-    const int32_t* drafts, const float* draft_q_stats, const void* prev_logits, int prev_rows,
-    const int32_t* prev_mask_row0, int C, int T, int N, float temperature, int proposal_mode,
-    uint64_t seed, uint64_t step, int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out,
-    int32_t* n_commit, int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
-    int32_t* next_mask_row0, float* row_stats, float* dbg, void* workspace,
-    size_t workspace_bytes, int32_t* status, void* stream_) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+namespace {
+
+// Checks the accept call's arguments, carves its workspace and fills the
+// kernels' parameters (part_given = 0).
+idlm_status accept_prepare(acc::Params& p, DeviceInfo& dev, const void* logits, int dtype, int V,
+                           const int32_t* qo_indptr, const uint8_t* mode, const int32_t* drafts,
+                           const float* draft_q_stats, const void* prev_logits, int prev_rows,
+                           const int32_t* prev_mask_row0, int C, int T, int N, float temperature,
+                           int proposal_mode, uint64_t seed, uint64_t step, int32_t* n_accepted,
+                           int32_t* out_tokens, int32_t* n_out, int32_t* n_commit,
+                           int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+                           int32_t* next_mask_row0, float* row_stats, float* dbg, void* workspace,
+                           size_t workspace_bytes, int32_t* status) {
   if (!logits || !qo_indptr || !mode || !drafts || !draft_q_stats || !prev_logits ||
       !prev_mask_row0 || !n_accepted || !out_tokens || !n_out || !n_commit || !next_drafts ||
       !next_q_stats || !next_mode || !next_mask_row0 || !status)
@@ -1128,10 +1174,8 @@ extern "C" idlm_status idlm_isd_accept(
   // bulk copies and vector loads start on 16-byte boundaries
   if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(prev_logits)) & 15)
     return IDLM_ERR_INVALID_ARG;
-  acc::Params p;
   if (!workspace || workspace_bytes < acc::workspace_bytes(C, T, V, dtype, nullptr, nullptr))
     return IDLM_ERR_WORKSPACE;
-  DeviceInfo dev;
   if (!current_device_info(&dev)) return IDLM_ERR_CUDA;
   acc::workspace_bytes(C, T, V, dtype, &p, workspace);
   p.logits = logits;
@@ -1165,8 +1209,95 @@ extern "C" idlm_status idlm_isd_accept(
   p.propose = proposal_mode;
   p.prev_rows = prev_rows;
   p.s2 = p.greedy ? 1.f : kLog2e / temperature;
+  p.part_given = 0;
+  return IDLM_OK;
+}
+
+idlm_status accept_launch(const acc::Params& p, const DeviceInfo& dev, int dtype,
+                          cudaStream_t stream) {
   if (dtype == IDLM_BF16) return acc::launch<__nv_bfloat16>(p, dev.device, dev.sm_count, stream);
   return acc::launch<float>(p, dev.device, dev.sm_count, stream);
+}
+
+}  // namespace
+
+extern "C" idlm_status idlm_isd_accept(
+    const void* logits, int dtype, int V, const int32_t* qo_indptr, const uint8_t* mode,
+    const int32_t* drafts, const float* draft_q_stats, const void* prev_logits, int prev_rows,
+    const int32_t* prev_mask_row0, int C, int T, int N, float temperature, int proposal_mode,
+    uint64_t seed, uint64_t step, int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out,
+    int32_t* n_commit, int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+    int32_t* next_mask_row0, float* row_stats, float* dbg, void* workspace,
+    size_t workspace_bytes, int32_t* status, void* stream) {
+  acc::Params p;
+  DeviceInfo dev;
+  const idlm_status rc = accept_prepare(
+      p, dev, logits, dtype, V, qo_indptr, mode, drafts, draft_q_stats, prev_logits, prev_rows,
+      prev_mask_row0, C, T, N, temperature, proposal_mode, seed, step, n_accepted, out_tokens,
+      n_out, n_commit, next_drafts, next_q_stats, next_mode, next_mask_row0, row_stats, dbg,
+      workspace, workspace_bytes, status);
+  if (rc != IDLM_OK) return rc;
+  return accept_launch(p, dev, dtype, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------- fused LM head + accept
+//
+// The forward pass's last product and the accept step in one call: the LM
+// head's GEMM writes the logits once and, in the same epilogue, the softmax
+// statistics of every logits row per 128-entry tile of the vocabulary; a
+// small kernel merges them into the accept's per-chunk records, and the
+// accept runs on them without its own pass over the logits (kernel 1 only
+// gathers the requests' inputs).  The logits are still written: the draws
+// (inverse-CDF searches of one chunk, the residual of a rejected draft) read
+// the rows and chunks they need from them.
+
+extern "C" size_t idlm_lm_head_accept_workspace_size(int C, int T, int N, int H, int V) {
+  if (C <= 0 || T <= 0 || N < 2 || H <= 0 || V <= 0) return 0;
+  Carver cv(nullptr);
+  cv.take<uint8_t>(acc::workspace_bytes(C, T, V, IDLM_BF16, nullptr, nullptr));
+  cv.take<acc::Partial>(static_cast<size_t>(T) * ((V + acc::kLmTile - 1) / acc::kLmTile));
+  cv.take<uint8_t>(lm_head_gemm_workspace(T, H, V));
+  return cv.used;
+}
+
+extern "C" idlm_status idlm_lm_head_accept(
+    const void* hidden, const void* w_vocab, int H, void* logits, int V,
+    const int32_t* qo_indptr, const uint8_t* mode, const int32_t* drafts,
+    const float* draft_q_stats, const void* prev_logits, int prev_rows,
+    const int32_t* prev_mask_row0, int C, int T, int N, float temperature, int proposal_mode,
+    uint64_t seed, uint64_t step, int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out,
+    int32_t* n_commit, int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+    int32_t* next_mask_row0, float* row_stats, float* dbg, void* workspace,
+    size_t workspace_bytes, int32_t* status, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!hidden || !w_vocab || !logits) return IDLM_ERR_INVALID_ARG;
+  if (H <= 0 || H % 8) return IDLM_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < idlm_lm_head_accept_workspace_size(C, T, N, H, V))
+    return IDLM_ERR_WORKSPACE;
+  Carver cv(workspace);
+  void* acc_ws = cv.take<uint8_t>(acc::workspace_bytes(C, T, V, IDLM_BF16, nullptr, nullptr));
+  const int tiles = (V + acc::kLmTile - 1) / acc::kLmTile;
+  acc::Partial* tstat = cv.take<acc::Partial>(static_cast<size_t>(T) * tiles);
+  const size_t gemm_bytes = lm_head_gemm_workspace(T, H, V);
+  void* gemm_ws = cv.take<uint8_t>(gemm_bytes);
+  acc::Params p;
+  DeviceInfo dev;
+  idlm_status rc = accept_prepare(
+      p, dev, logits, IDLM_BF16, V, qo_indptr, mode, drafts, draft_q_stats, prev_logits,
+      prev_rows, prev_mask_row0, C, T, N, temperature, proposal_mode, seed, step, n_accepted,
+      out_tokens, n_out, n_commit, next_drafts, next_q_stats, next_mode, next_mask_row0,
+      row_stats, dbg, acc_ws, acc::workspace_bytes(C, T, V, IDLM_BF16, nullptr, nullptr), status);
+  if (rc != IDLM_OK) return rc;
+  // logits = H W^T and the tile statistics of every row
+  rc = lm_head_gemm(hidden, w_vocab, T, H, V, logits, gemm_ws, gemm_bytes, tstat, p.s2,
+                    p.greedy, status, stream);
+  if (rc != IDLM_OK) return rc;
+  const long long warps = static_cast<long long>(T) * p.CH;
+  acc::lm_combine_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
+      tstat, tiles, p.part, T, p.CH, p.greedy);
+  if (cudaGetLastError() != cudaSuccess) return IDLM_ERR_CUDA;
+  p.part_given = 1;
+  return accept_launch(p, dev, IDLM_BF16, stream);
 }
 
 // ------------------------------------------------------- allocation-free entry

@@ -55,4 +55,13 @@ struct Carver {
 
 inline idlm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? IDLM_OK : IDLM_ERR_CUDA; }
 
+// The LM-head GEMM of the fused LM-head + accept call (lora.cu): logits =
+// H W^T in bf16, [T][V], and the softmax statistics of every logits row per
+// 128-entry tile of the vocabulary, 16-byte records (max z, sum, max x,
+// first argmax) at tile_stats[row * ceil(V / 128) + tile].
+size_t lm_head_gemm_workspace(int T, int H, int V);
+idlm_status lm_head_gemm(const void* h, const void* w, int T, int H, int V, void* logits,
+                         void* workspace, size_t workspace_bytes, void* tile_stats, float s2,
+                         int greedy, int32_t* status, cudaStream_t stream);
+
 }  // namespace idlm

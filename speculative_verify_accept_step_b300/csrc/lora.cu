@@ -76,6 +76,15 @@ constexpr int kMaxGroups = 4;
 constexpr int kMaxRank = 128;
 constexpr int kPadW = 64;                  // adapter columns per K step
 
+// Softmax statistics of one token row over one tile's 128 weight rows (the
+// vocabulary entries of an LM head), taken from the bf16 values written to
+// Y: m = max of z = x s2 (greedy: max x), s = sum of 2^(z - m) (greedy: 1),
+// amax = max x, aidx = the first index of the maximum (or INT_MAX).
+struct __align__(16) TileStat {
+  float m, s, amax;
+  int aidx;
+};
+
 struct Params {
   __nv_bfloat16* y;
   float4* part;             // [grid][2][m16 / 4][128] fp32 partial tiles (two slots per CTA)
@@ -102,6 +111,9 @@ struct Params {
   int test_stall;         // failure-detection test switch (see the entry point)
   const uint8_t* rs_gate; // or null: Y row m is scaled by (rs_gate[m] ? rs_scale : 0)
   float rs_scale;
+  TileStat* stats;        // or null: [M][tiles] statistics of every token row per tile
+  float s2;               // log2(e) / temperature (statistics only)
+  int greedy;             // temperature 0: statistics of the raw values
 };
 
 // Factor of token row m of Y (1 without row scaling).
@@ -499,6 +511,55 @@ inline size_t smem_bytes(int stages, uint32_t stage_bytes) {
   return 1024 + bar_offset(stages, stage_bytes) + kBarBytes;
 }
 
+// Statistics of one token row over one tile, spread over G consecutive lanes
+// (G = 8 or 4) that each hold `cnt` consecutive entries of the row (bf16, in
+// shared memory at `vals`, vocabulary index n0 of the first); entries with
+// index >= N are left out.  The lane with (lane % G) == 0 writes the record.
+template <int G>
+__device__ __forceinline__ void tile_stat(int N, float s2, int greedy, const __nv_bfloat16* vals,
+                                          int cnt, int n0, TileStat* dst) {
+  const int lane = threadIdx.x & 31;
+  float bx = -__builtin_inff();
+  int bi = 0x7fffffff;
+  for (int e = 0; e < cnt; ++e)
+    if (n0 + e < N) {
+      const float x = __bfloat162float(vals[e]);
+      if (x > bx) {
+        bx = x;
+        bi = n0 + e;
+      }
+    }
+  float sum = 0.f;
+  const float mz = bx * s2;
+  if (!greedy && bi != 0x7fffffff)
+    for (int e = 0; e < cnt; ++e)
+      if (n0 + e < N) sum += fast_exp2(fmaf(__bfloat162float(vals[e]), s2, -mz));
+  // the G lanes' (max, first index), then the sum rescaled to the common max
+  float BX = bx;
+  int BI = bi;
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) {
+    const float ox = __shfl_xor_sync(0xffffffffu, BX, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, BI, o);
+    if (ox > BX || (ox == BX && oi < BI)) {
+      BX = ox;
+      BI = oi;
+    }
+  }
+  const float MZ = BX * s2;
+  float S = (greedy || bi == 0x7fffffff) ? 0.f : sum * fast_exp2(mz - MZ);
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  if ((lane % G) == 0 && dst) {
+    TileStat t;
+    t.m = greedy ? BX : MZ;
+    t.s = greedy ? 1.f : S;
+    t.amax = BX;
+    t.aidx = BI;
+    *dst = t;
+  }
+}
+
 // Epilogue of a tile whose K sum this CTA holds whole: Y (bf16) for the
 // tile's 128 weight rows, through the 16-token staging buffer with 16-byte
 // stores of whole 256-byte rows.  Thread `row` owns weight row tile*128+row.
@@ -516,6 +577,14 @@ __device__ __noinline__ void store_y_direct(const Params& p, uint32_t taddr, int
             __uint_as_float(ra[16 * h + j]) *
             row_factor(p.rs_gate, p.rs_scale, min(c0 + 16 * h + j, p.M - 1)));
       epi_sync();
+      if (p.stats) {
+        // 16 token rows x the tile's 128 entries: 8 lanes per row, 16 entries each
+        const int j = et >> 3, q8 = et & 7;
+        const int m = c0 + 16 * h + j;
+        TileStat* dst = p.stats + static_cast<size_t>(min(m, p.M - 1)) * p.tiles + n_base / kTileN;
+        tile_stat<8>(p.N, p.s2, p.greedy, ystage + j * kTileN + q8 * 16, 16, n_base + q8 * 16,
+                     m < p.M ? dst : nullptr);
+      }
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
         const int idx = it * 128 + et;
@@ -553,6 +622,14 @@ __device__ __noinline__ void store_y_tma(const Params& p, uint32_t taddr, int n_
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
+  if (p.stats) {
+    // every token row x the tile's 128 entries: 8 lanes per row, 16 entries each
+    for (int g0 = 0; g0 < p.m16; g0 += 16) {
+      const int m = g0 + (et >> 3), q8 = et & 7;
+      TileStat* dst = m < p.M ? p.stats + static_cast<size_t>(m) * p.tiles + n_base / kTileN : nullptr;
+      tile_stat<8>(p.N, p.s2, p.greedy, ytile + m * kTileN + q8 * 16, 16, n_base + q8 * 16, dst);
+    }
+  }
   if (et == 0) {
     for (int rb0 = 0; rb0 < p.m16; rb0 += kYBoxRows) tma_store_2d(y_map, ytile + rb0 * kTileN, n_base, rb0);
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -785,6 +862,9 @@ struct FParams {
   int S, G, M, N, m16, sk_tiles;
   const uint8_t* rs_gate;   // row scaling as in Params
   float rs_scale;
+  TileStat* stats;          // statistics as in Params (or null)
+  float s2;
+  int greedy, tiles;
 };
 
 __device__ __forceinline__ long long fx_begin(const FParams& f, int c) {
@@ -826,13 +906,21 @@ __global__ void __launch_bounds__(128) lora_fixup_kernel(const FParams f) {
     }
   }
   const int n = t * kTileN + row;
-  if (n >= f.N) return;
+  __shared__ __nv_bfloat16 sy[32][kTileN];   // this CTA's 32 token rows of the tile
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int m = ch * 32 + j;
-    if (m < f.M)
-      f.y[static_cast<size_t>(m) * f.N + n] =
-          __float2bfloat16_rn(v[j] * row_factor(f.rs_gate, f.rs_scale, m));
+    const __nv_bfloat16 yv =
+        __float2bfloat16_rn(m < f.M ? v[j] * row_factor(f.rs_gate, f.rs_scale, m) : 0.f);
+    sy[j][row] = yv;
+    if (m < f.M && n < f.N) f.y[static_cast<size_t>(m) * f.N + n] = yv;
+  }
+  if (f.stats) {
+    // 32 token rows x the tile's 128 entries: 4 lanes per row, 32 entries each
+    __syncthreads();
+    const int j = row >> 2, q4 = row & 3, m = ch * 32 + j;
+    TileStat* dst = m < f.M ? f.stats + static_cast<size_t>(m) * f.tiles + t : nullptr;
+    tile_stat<4>(f.N, f.s2, f.greedy, &sy[j][q4 * 32], 32, t * kTileN + q4 * 32, dst);
   }
 }
 
@@ -947,6 +1035,9 @@ struct GemmArgs {
   const uint8_t* rs_gate;   // or null
   float rs_scale;
   bool test_stall;
+  lora::TileStat* stats;    // or null: softmax statistics of Y's rows per tile (LM head)
+  float s2;
+  int greedy;
 };
 
 // One GEMM launch over a slice of <= 448 token rows, then the fix-up kernel
@@ -992,6 +1083,9 @@ idlm_status launch_gemm(const GemmArgs& a, const LoraPlan& pl, int stages, size_
   p.stage_bytes = pl.stage_bytes;
   p.wait_ns = a.test_stall ? 20000000ull : kWaitNs;
   p.test_stall = a.test_stall ? 1 : 0;
+  p.stats = a.stats;
+  p.s2 = a.s2;
+  p.greedy = a.greedy;
   CUtensorMap ym;
   if (p.ytma) {
     const uint64_t ydims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(a.Ms)};
@@ -1030,6 +1124,10 @@ idlm_status launch_gemm(const GemmArgs& a, const LoraPlan& pl, int stages, size_
     f.sk_tiles = pl.sk_tiles;
     f.rs_gate = a.rs_gate;
     f.rs_scale = a.rs_scale;
+    f.stats = a.stats;
+    f.s2 = a.s2;
+    f.greedy = a.greedy;
+    f.tiles = pl.tiles;
     cudaLaunchConfig_t fc = {};
     fc.gridDim = dim3(pl.sk_tiles * ((pl.m16 + 31) / 32));
     fc.blockDim = dim3(128);
@@ -1050,7 +1148,8 @@ idlm_status launch_gemm(const GemmArgs& a, const LoraPlan& pl, int stages, size_
 idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, const void* lora_b,
                             const uint8_t* row_gate, float lora_scale, int M, int K, int N, int r,
                             int ngroups, const int* group_rows, void* y, void* workspace,
-                            size_t workspace_bytes, int32_t* status, cudaStream_t stream) {
+                            size_t workspace_bytes, int32_t* status, cudaStream_t stream,
+                            lora::TileStat* stats = nullptr, float s2 = 0.f, int greedy = 0) {
   if (!x || !w || !y || !status) return IDLM_ERR_INVALID_ARG;
   if (r > 0 && (!lora_a || !lora_b || !row_gate)) return IDLM_ERR_INVALID_ARG;
   if (M <= 0 || K <= 0 || N <= 0 || r < 0 || ngroups < 1) return IDLM_ERR_INVALID_ARG;
@@ -1201,9 +1300,11 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
       if (cudaGetLastError() != cudaSuccess) return IDLM_ERR_CUDA;
     }
 
+    const int tiles = (N + lora::kTileN - 1) / lora::kTileN;
     const GemmArgs ga{xs, Ms, K, w, N, r, ngroups, gend_rows, R64, wm, xm1, xm2, bm, tm1, tm2,
                       yb + static_cast<size_t>(m0) * N, reinterpret_cast<float4*>(wsb + wl.part),
-                      nullptr, 0.f, test_stall};
+                      nullptr, 0.f, test_stall,
+                      stats ? stats + static_cast<size_t>(m0) * tiles : nullptr, s2, greedy};
     const idlm_status rc = launch_gemm(ga, pl, stages, smem, status, stream);
     if (rc != IDLM_OK) return rc;
   }
@@ -1241,3 +1342,21 @@ extern "C" idlm_status idlm_gated_lora_grouped(const void* x, const void* w, con
                          group_rows, y, workspace, workspace_bytes, status,
                          static_cast<cudaStream_t>(stream));
 }
+
+namespace idlm {
+
+// The LM head of the fused LM-head + accept call: logits = H W^T (bf16) with
+// the softmax statistics of every row per 128-entry tile of the vocabulary
+// (TileStat records, [T][ceil(V / 128)]) taken in the same epilogue.
+size_t lm_head_gemm_workspace(int T, int H, int V) { return ws_layout(T, H, V, 0, 1).total; }
+
+idlm_status lm_head_gemm(const void* h, const void* w, int T, int H, int V, void* logits,
+                         void* workspace, size_t workspace_bytes, void* tile_stats, float s2,
+                         int greedy, int32_t* status, cudaStream_t stream) {
+  if (!tile_stats) return IDLM_ERR_INVALID_ARG;
+  return gated_lora_impl(h, w, nullptr, nullptr, nullptr, 0.f, T, H, V, 0, 1, nullptr, logits,
+                         workspace, workspace_bytes, status, stream,
+                         static_cast<lora::TileStat*>(tile_stats), s2, greedy);
+}
+
+}  // namespace idlm
