@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--no-loop", action="store_true", help="skip the decode-loop leg")
     ap.add_argument("--no-ragged", action="store_true",
                     help="skip the ragged 1k-32k workload leg")
-    ap.add_argument("--leg", default="step", choices=["step", "lora", "layer", "loop"],
+    ap.add_argument("--no-lmhead", action="store_true", help="skip the fused LM-head leg")
+    ap.add_argument("--leg", default="step", choices=["step", "lora", "layer", "loop", "lmhead"],
                     help="lora: only the gated-LoRA projections (prints their JSON)")
     ap.add_argument("--lora-reps", type=int, default=20)
     ap.add_argument("--lora-rank", type=int, default=None)
@@ -183,6 +184,101 @@ def layer_leg(dev, reps=10):
         torch.cuda.empty_cache()
     res["alpha_pages"] = 1.12
     return res
+
+
+def lmhead_leg(dev, reps=20):
+    """The LM head fused with the accept step (idlm_lm_head_accept) against
+    the two calls it replaces: the same tcgen05 GEMM writing the logits
+    (idlm_gated_lora without an adapter), then idlm_isd_accept with its own
+    pass over them.  The headline batch: 64 requests, N = 4 (448 rows of a
+    FULL step), hidden 4096, V = 151936; random bf16 hidden states and LM-head
+    weights (synthetic), the drafts those weights propose at a FRESH step
+    before.  Both sides are timed with CUDA events over `reps` calls each."""
+    import speculative_verify_accept_step_b300 as L
+    C, N, H, V = 64, 4, 4096, 151936
+    M = N - 1
+    g = torch.Generator(device=dev).manual_seed(5)
+    h0 = torch.randn(C * N, H, device=dev, generator=g).bfloat16()
+    h1 = torch.randn(C * (2 * N - 1), H, device=dev, generator=g)
+    for k in range(1, N):   # clean row k - 1 close to the FRESH step's MASK row k
+        h1[k - 1::2 * N - 1] = h0[k::N].float() + 0.35 * torch.randn(C, H, device=dev, generator=g)
+    h1 = h1.bfloat16()
+    w = (torch.randn(V, H, device=dev, generator=g) * (2.0 / H ** 0.5)).bfloat16()
+    i32 = dict(dtype=torch.int32, device=dev)
+    qo0 = torch.arange(0, C * N + 1, N, **i32)
+    qo1 = torch.arange(0, C * (2 * N - 1) + 1, 2 * N - 1, **i32)
+    l0 = torch.empty(C * N, V, dtype=torch.bfloat16, device=dev)
+    l1 = torch.empty(C * (2 * N - 1), V, dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, **i32)
+
+    def outs():
+        return dict(n_accepted=torch.empty(C, **i32), out_tokens=torch.empty((C, N), **i32),
+                    n_out=torch.empty(C, **i32), n_commit=torch.empty(C, **i32),
+                    next_drafts=torch.empty((C, M), **i32),
+                    next_q_stats=torch.empty((C, M, 2), dtype=torch.float32, device=dev),
+                    next_mode=torch.empty(C, dtype=torch.uint8, device=dev),
+                    next_mask_row0=torch.empty(C, **i32))
+    ws = torch.empty(L.idlm_lm_head_accept_workspace_size(C, C * (2 * N - 1), N, H, V),
+                     dtype=torch.uint8, device=dev)
+    o0, o1 = outs(), outs()
+    L.idlm_lm_head_accept(h0, w, l0, qo0, torch.zeros(C, dtype=torch.uint8, device=dev),
+                          torch.full((C, M), -1, **i32),
+                          torch.zeros((C, M, 2), dtype=torch.float32, device=dev), l0,
+                          torch.zeros(C, **i32), N, 1.0, L.PROPOSE_ARGMAX, 0, 0,
+                          o0["n_accepted"], o0["out_tokens"], o0["n_out"], o0["n_commit"],
+                          o0["next_drafts"], o0["next_q_stats"], o0["next_mode"],
+                          o0["next_mask_row0"], ws, st)
+
+    def fused():
+        L.idlm_lm_head_accept(h1, w, l1, qo1, o0["next_mode"], o0["next_drafts"],
+                              o0["next_q_stats"], l0, o0["next_mask_row0"], N, 1.0,
+                              L.PROPOSE_ARGMAX, 0, 1, o1["n_accepted"], o1["out_tokens"],
+                              o1["n_out"], o1["n_commit"], o1["next_drafts"], o1["next_q_stats"],
+                              o1["next_mode"], o1["next_mask_row0"], ws, st)
+    T1 = C * (2 * N - 1)
+    empty_a = torch.zeros((0, H), dtype=torch.bfloat16, device=dev)
+    empty_b = torch.zeros((V, 0), dtype=torch.bfloat16, device=dev)
+    gate = torch.zeros(T1, dtype=torch.uint8, device=dev)
+    gws = torch.empty(L.idlm_gated_lora_workspace_size(T1, H, V, 0), dtype=torch.uint8,
+                      device=dev)
+    aws = torch.empty(L.idlm_isd_accept_workspace_size(C, T1, N, V), dtype=torch.uint8,
+                      device=dev)
+
+    def gemm():
+        L.idlm_gated_lora(h1, w, empty_a, empty_b, gate, 1.0, l1, gws, st)
+
+    def accept():
+        L.idlm_isd_accept(l1, qo1, o0["next_mode"], o0["next_drafts"], o0["next_q_stats"], l0,
+                          o0["next_mask_row0"], N, 1.0, L.PROPOSE_ARGMAX, 0, 1, o1["n_accepted"],
+                          o1["out_tokens"], o1["n_out"], o1["n_commit"], o1["next_drafts"],
+                          o1["next_q_stats"], o1["next_mode"], o1["next_mask_row0"], aws, st)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3
+    t_fused = timed(fused)
+    t_gemm = timed(gemm)
+    t_acc = timed(accept)
+    t_pair = timed(lambda: (gemm(), accept()))
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    flop = 2.0 * T1 * H * V
+    return {"requests": C, "N": N, "rows": T1, "hidden": H, "V": V,
+            "fused_us": t_fused, "gemm_us": t_gemm, "accept_us": t_acc,
+            "gemm_then_accept_us": t_pair, "saved_us": t_pair - t_fused,
+            "gemm_TFLOP/s": flop / (t_gemm * 1e-6) / 1e12,
+            "fused_TFLOP/s": flop / (t_fused * 1e-6) / 1e12,
+            "logits_bytes": T1 * V * 2,
+            "note": "logits written once by the GEMM in both; the fused call takes the "
+                    "accept's vocabulary statistics in the GEMM's epilogue instead of a "
+                    "second pass over the logits"}
 
 
 def loop_leg(dev, steps=200, warm=10, target=0.9):
@@ -539,6 +635,12 @@ def run_ours(args):
             layer = layer_leg(dev)
         except Exception as e:   # reported, never fatal to the step's line
             layer = {"error": str(e)[:300]}
+    lmhead = None
+    if not args.profile_run and not args.no_lmhead:
+        try:
+            lmhead = lmhead_leg(dev)
+        except Exception as e:   # reported, never fatal to the step's line
+            lmhead = {"error": str(e)[:300]}
     loop = None
     if not args.profile_run and not args.no_loop:
         try:
@@ -593,6 +695,7 @@ def run_ours(args):
         "lora": lora,
         "layer": layer,
         "loop": loop,
+        "lm_head": lmhead,
         "workloads": {"isd_c64_n4_ctx1k_32k": ragged} if ragged else None,
     }
     print(json.dumps(line))
@@ -979,6 +1082,9 @@ def main():
         build()
     if args.leg == "layer":
         print(json.dumps(layer_leg(torch.device("cuda", 0))))
+        return
+    if args.leg == "lmhead":
+        print(json.dumps(lmhead_leg(torch.device("cuda", 0))))
         return
     if args.leg == "loop":
         torch.cuda.set_device(0)

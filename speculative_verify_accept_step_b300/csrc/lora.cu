@@ -512,28 +512,28 @@ inline size_t smem_bytes(int stages, uint32_t stage_bytes) {
 }
 
 // Statistics of one token row over one tile, spread over G consecutive lanes
-// (G = 8 or 4) that each hold `cnt` consecutive entries of the row (bf16, in
-// shared memory at `vals`, vocabulary index n0 of the first); entries with
-// index >= N are left out.  The lane with (lane % G) == 0 writes the record.
-template <int G>
-__device__ __forceinline__ void tile_stat(int N, float s2, int greedy, const __nv_bfloat16* vals,
-                                          int cnt, int n0, TileStat* dst) {
+// (G = 8 or 4) that each hold CNT consecutive entries of the row in x
+// (vocabulary index n0 of the first); entries with index >= N are left out.
+// The lane with (lane % G) == 0 writes the record (where dst is not null).
+template <int G, int CNT>
+__device__ __forceinline__ void tile_stat(int N, float s2, int greedy, const float (&x)[CNT],
+                                          int n0, TileStat* dst) {
   const int lane = threadIdx.x & 31;
   float bx = -__builtin_inff();
   int bi = 0x7fffffff;
-  for (int e = 0; e < cnt; ++e)
-    if (n0 + e < N) {
-      const float x = __bfloat162float(vals[e]);
-      if (x > bx) {
-        bx = x;
-        bi = n0 + e;
-      }
+#pragma unroll
+  for (int e = 0; e < CNT; ++e)
+    if (n0 + e < N && x[e] > bx) {
+      bx = x[e];
+      bi = n0 + e;
     }
-  float sum = 0.f;
   const float mz = bx * s2;
-  if (!greedy && bi != 0x7fffffff)
-    for (int e = 0; e < cnt; ++e)
-      if (n0 + e < N) sum += fast_exp2(fmaf(__bfloat162float(vals[e]), s2, -mz));
+  float sum = 0.f;
+  if (!greedy && bi != 0x7fffffff) {
+#pragma unroll
+    for (int e = 0; e < CNT; ++e)
+      if (n0 + e < N) sum += fast_exp2(fmaf(x[e], s2, -mz));
+  }
   // the G lanes' (max, first index), then the sum rescaled to the common max
   float BX = bx;
   int BI = bi;
@@ -560,6 +560,24 @@ __device__ __forceinline__ void tile_stat(int N, float s2, int greedy, const __n
   }
 }
 
+// Eight bf16 values (16 bytes of shared memory) as floats.
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* src, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(src);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(w[k] << 16);
+    x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+  }
+}
+
+// The Y staging buffer holds 16 token rows of the tile's 128 entries, the
+// 16-byte groups of row j permuted by j (group g at g ^ j), so that the
+// statistics' 16-byte reads of a row spread over the banks.
+__device__ __forceinline__ int ystage_at(int j, int col) {
+  return j * kTileN + ((((col >> 3) ^ j) & 15) << 3) + (col & 7);
+}
+
 // Epilogue of a tile whose K sum this CTA holds whole: Y (bf16) for the
 // tile's 128 weight rows, through the 16-token staging buffer with 16-byte
 // stores of whole 256-byte rows.  Thread `row` owns weight row tile*128+row.
@@ -573,7 +591,7 @@ __device__ __noinline__ void store_y_direct(const Params& p, uint32_t taddr, int
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        ystage[j * kTileN + row] = __float2bfloat16_rn(
+        ystage[ystage_at(j, row)] = __float2bfloat16_rn(
             __uint_as_float(ra[16 * h + j]) *
             row_factor(p.rs_gate, p.rs_scale, min(c0 + 16 * h + j, p.M - 1)));
       epi_sync();
@@ -581,9 +599,11 @@ __device__ __noinline__ void store_y_direct(const Params& p, uint32_t taddr, int
         // 16 token rows x the tile's 128 entries: 8 lanes per row, 16 entries each
         const int j = et >> 3, q8 = et & 7;
         const int m = c0 + 16 * h + j;
+        float x[16];
+        load8_bf16(ystage + ystage_at(j, q8 * 16), x);
+        load8_bf16(ystage + ystage_at(j, q8 * 16 + 8), x + 8);
         TileStat* dst = p.stats + static_cast<size_t>(min(m, p.M - 1)) * p.tiles + n_base / kTileN;
-        tile_stat<8>(p.N, p.s2, p.greedy, ystage + j * kTileN + q8 * 16, 16, n_base + q8 * 16,
-                     m < p.M ? dst : nullptr);
+        tile_stat<8, 16>(p.N, p.s2, p.greedy, x, n_base + q8 * 16, m < p.M ? dst : nullptr);
       }
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
@@ -591,7 +611,7 @@ __device__ __noinline__ void store_y_direct(const Params& p, uint32_t taddr, int
         const int rr = idx >> 4, c8 = (idx & 15) * 8;
         const int m = c0 + 16 * h + rr, n0 = n_base + c8;
         if (m < p.M) {
-          const __nv_bfloat16* src = ystage + rr * kTileN + c8;
+          const __nv_bfloat16* src = ystage + ystage_at(rr, c8);
           __nv_bfloat16* out = p.y + static_cast<size_t>(m) * p.N + n0;
           if (p.yvec && n0 + 8 <= p.N) {
             *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
@@ -626,8 +646,11 @@ __device__ __noinline__ void store_y_tma(const Params& p, uint32_t taddr, int n_
     // every token row x the tile's 128 entries: 8 lanes per row, 16 entries each
     for (int g0 = 0; g0 < p.m16; g0 += 16) {
       const int m = g0 + (et >> 3), q8 = et & 7;
+      float x[16];
+      load8_bf16(ytile + m * kTileN + q8 * 16, x);
+      load8_bf16(ytile + m * kTileN + q8 * 16 + 8, x + 8);
       TileStat* dst = m < p.M ? p.stats + static_cast<size_t>(m) * p.tiles + n_base / kTileN : nullptr;
-      tile_stat<8>(p.N, p.s2, p.greedy, ytile + m * kTileN + q8 * 16, 16, n_base + q8 * 16, dst);
+      tile_stat<8, 16>(p.N, p.s2, p.greedy, x, n_base + q8 * 16, dst);
     }
   }
   if (et == 0) {
@@ -919,8 +942,11 @@ __global__ void __launch_bounds__(128) lora_fixup_kernel(const FParams f) {
     // 32 token rows x the tile's 128 entries: 4 lanes per row, 32 entries each
     __syncthreads();
     const int j = row >> 2, q4 = row & 3, m = ch * 32 + j;
+    float x[32];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) load8_bf16(&sy[j][q4 * 32 + 8 * k], x + 8 * k);
     TileStat* dst = m < f.M ? f.stats + static_cast<size_t>(m) * f.tiles + t : nullptr;
-    tile_stat<4>(f.N, f.s2, f.greedy, &sy[j][q4 * 32], 32, t * kTileN + q4 * 32, dst);
+    tile_stat<4, 32>(f.N, f.s2, f.greedy, x, t * kTileN + q4 * 32, dst);
   }
 }
 
