@@ -997,7 +997,9 @@ struct LoraPlan {
 // step of the 128 x 448 tile about 0.65 us (the MMAs near the measured bf16
 // rate); an fp32 partial tile about 2 us to write, a whole tile's Y about
 // 3 us, and the fix-up kernel about 3 us plus its share of the partial
-// bytes.  A quarter of a K step and the epilogues scale with the tokens.  A
+// bytes plus ~0.8 us per CTA whose partial a split tile adds (the adds
+// of one tile are a chain of L2 round trips).  A quarter of a K step and the
+// epilogues scale with the tokens.  A
 // grid of G CTAs holds floor(tiles / G) whole tiles each and splits the
 // other tiles' units evenly.
 LoraPlan plan_for(int M, int K, int N, int r, int grid_cap) {
@@ -1037,8 +1039,12 @@ LoraPlan plan_for(int M, int K, int N, int r, int grid_cap) {
     const double part_mb =
         cut ? static_cast<double>(std::min<long long>(2 * G, skt + G)) * pl.m16 * lora::kTileN * 4 / 1e6
             : 0.0;
+    // the fix-up adds a split tile's partials one contributing CTA after
+    // another (an L2 round trip each), so deep splits of few tiles cost a
+    // serial chain of ~0.8 us per part
+    const double chain = cut ? 0.8 * static_cast<double>((G + skt - 1) / std::max(skt, 1) + 1) : 0.0;
     const double t = (dp * pl.S + sk_per) * step + (dp ? 3.0 * f : 0.0) +
-                     (cut ? 2.0 * f + 3.0 + part_mb / (0.1 * G) : (usk ? 3.0 * f : 0.0));
+                     (cut ? 2.0 * f + 3.0 + part_mb / (0.1 * G) + chain : (usk ? 3.0 * f : 0.0));
     if (t < best * 0.98) {
       best = t;
       pl.grid = static_cast<int>(G);
