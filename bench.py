@@ -30,7 +30,9 @@ import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "ISD accepted tokens/s at C=64,N=4; attention+accept HBM GB/s vs B300 peak"
-LAUNCHES_PER_STEP = 5
+# library launches per timed step: attention 1, accept 3 (the KV commit runs
+# as work items of the accept's residual kernel); 5 with --separate-commit
+LAUNCHES_PER_STEP = 4
 
 
 def parse():
@@ -47,6 +49,9 @@ def parse():
     ap.add_argument("--no-ragged", action="store_true",
                     help="skip the ragged 1k-32k workload leg")
     ap.add_argument("--no-lmhead", action="store_true", help="skip the fused LM-head leg")
+    ap.add_argument("--separate-commit", action="store_true",
+                    help="time the step as idlm_isd_accept then idlm_kv_commit (5 launches) "
+                         "instead of idlm_isd_accept_commit (4)")
     ap.add_argument("--leg", default="step", choices=["step", "lora", "layer", "loop", "lmhead"],
                     help="lora: only the gated-LoRA projections (prints their JSON)")
     ap.add_argument("--lora-reps", type=int, default=20)
@@ -339,7 +344,9 @@ def loop_leg(dev, steps=200, warm=10, target=0.9):
             "ms_per_step": ms / steps, "tokens_per_s": d["tokens"] / (ms * 1e-3),
             "model_ms_per_step": model_ms,
             "tokens_per_s_without_model": d["tokens"] / ((ms - model_ms * steps) * 1e-3),
-            "launches_per_step": 5,
+            # synth, attention, accept + commit, advance; kernels: synth 1,
+            # attention 1, accept 3 (the commit as its work items), advance 1
+            "api_calls_per_step": 4, "kernel_launches_per_step": 6,
             "note": "ms_per_step includes the synthetic model kernel (the step's logits, one "
                     "Philox4x32-10 per logit); model_ms_per_step is that kernel timed alone"}
 
@@ -528,6 +535,25 @@ class Step:
                               self.seq_out, self.k_new, self.v_new, self.qo, o["n_commit"],
                               self.status, releasable_from=self.releasable)
 
+    def accept_commit(self, o, step):
+        L, w = self.L, self.w
+        L.idlm_isd_accept_commit(self.logits1, self.qo1, self.mode1, self.drafts, self.dq,
+                                 self.logits0, self.prow, w.N, w.temperature, L.PROPOSE_ARGMAX,
+                                 0, step, o["n_accepted"], o["out_tokens"], o["n_out"],
+                                 o["n_commit"], o["next_drafts"], o["next_q_stats"],
+                                 o["next_mode"], o["next_mask_row0"], self.k_cache, self.v_cache,
+                                 self.page_table, self.seq_lens, self.seq_out, self.k_new,
+                                 self.v_new, self.acc_ws, self.status,
+                                 releasable_from=self.releasable)
+
+    def tail(self, o, step, fused=True):
+        """Accept and KV commit of the step: one call, or the two calls."""
+        if fused:
+            self.accept_commit(o, step)
+        else:
+            self.accept(o, step)
+            self.commit(o)
+
 
 def attention_bytes(w, seq_lens):
     """Algorithmic HBM bytes of one attention launch: every cached K/V byte
@@ -559,10 +585,10 @@ def run_ours(args):
     K, Wm = args.steps, args.warmup
     outs = [st.outs() for _ in range(K)]
     wo = st.outs()
+    fused = not args.separate_commit
     for i in range(Wm):
         st.attention()
-        st.accept(wo, 10_000_000 + i)
-        st.commit(wo)
+        st.tail(wo, 10_000_000 + i, fused)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     if not args.profile_run:
@@ -574,8 +600,7 @@ def run_ours(args):
     while time.time() - t_load < 0.6 and not args.profile_run:
         for _ in range(50):
             st.attention()
-            st.accept(wo, 20_000_000 + i)
-            st.commit(wo)
+            st.tail(wo, 20_000_000 + i, fused)
             i += 1
         torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
@@ -587,9 +612,13 @@ def run_ours(args):
         ev[k][0].record()
         st.attention()
         ev[k][1].record()
-        st.accept(outs[k], k + 1)
-        ev[k][2].record()
-        st.commit(outs[k])
+        if fused:
+            st.accept_commit(outs[k], k + 1)
+            ev[k][2].record()
+        else:
+            st.accept(outs[k], k + 1)
+            ev[k][2].record()
+            st.commit(outs[k])
         ev[k][3].record()
     e1.record()
     torch.cuda.synchronize()
@@ -610,6 +639,20 @@ def run_ours(args):
     att_gbs = a_bytes / (att_ms * 1e-3) / 1e9
     acc_gbs = c_bytes / (acc_ms * 1e-3) / 1e9
     both_gbs = (a_bytes + c_bytes) / ((att_ms + acc_ms) * 1e-3) / 1e9
+    separate = None
+    if fused and not args.profile_run:
+        # the two calls the fused one replaces, timed apart (not part of the value)
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(50)]
+        for k in range(50):
+            st.attention()
+            sev[k][0].record()
+            st.accept(wo, 30_000_000 + k)
+            sev[k][1].record()
+            st.commit(wo)
+            sev[k][2].record()
+        torch.cuda.synchronize()
+        separate = {"accept_us": sum(e[0].elapsed_time(e[1]) for e in sev) / 50 * 1e3,
+                    "commit_us": sum(e[1].elapsed_time(e[2]) for e in sev) / 50 * 1e3}
 
     e2e = None if args.profile_run else run_e2e(st, args.e2e_steps, ws)
     ragged = None
@@ -679,16 +722,18 @@ def run_ours(args):
         "kernels": {
             "attention": {"us": att_ms * 1e3, "GB/s": att_gbs, "frac": att_gbs / hbm},
             "accept": {"us": acc_ms * 1e3, "GB/s": acc_gbs, "frac": acc_gbs / hbm,
-                       "algorithmic_bytes": c_bytes},
-            "commit": {"us": com_ms * 1e3},
+                       "algorithmic_bytes": c_bytes, "includes_kv_commit": fused},
+            "commit": ({"us": com_ms * 1e3} if not fused else
+                       {"fused_into_accept": True, "separate_calls": separate}),
             "attention+accept": {"GB/s": both_gbs, "frac": both_gbs / hbm},
         },
         "tokens_per_step": n_out / K,
         "accepted_drafts_per_step": n_acc / K,
         "accepted_drafts_per_s": allreduce(float(n_acc), ws, _sum_op()) / (ms * 1e-3),
         # per step: paged_attn_kernel; vocab_stream_kernel, decide_kernel,
-        # work_kernel; commit_kernel (no memsets or copies)
-        "gpu_launches": LAUNCHES_PER_STEP * K,
+        # work_kernel (which also commits the KV rows); commit_kernel only with
+        # --separate-commit (no memsets or copies)
+        "gpu_launches": (LAUNCHES_PER_STEP + (0 if fused else 1)) * K,
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -744,14 +789,13 @@ def run_e2e(st, K, ws):
         L.idlm_isd_attention(d["q"], d["k_new"], d["v_new"], st.k_cache, st.v_cache,
                              d["page_table"], d["seq_lens"], d["qo"], st.out, st.att_ws,
                              st.status, max_rows=w.rows_full, sm_scale=st.sm_scale)
-        L.idlm_isd_accept(d["logits"], d["qo1"], d["mode"], d["drafts"], d["dq"], st.logits0,
-                          d["prow"], w.N, w.temperature, L.PROPOSE_ARGMAX, 0, base + k,
-                          o["n_accepted"], o["out_tokens"], o["n_out"], o["n_commit"],
-                          o["next_drafts"], o["next_q_stats"], o["next_mode"],
-                          o["next_mask_row0"], st.acc_ws, st.status)
-        L.idlm_kv_commit(st.k_cache, st.v_cache, d["page_table"], d["seq_lens"], seq_out,
-                         d["k_new"], d["v_new"], d["qo"], o["n_commit"], st.status,
-                         releasable_from=st.releasable)
+        L.idlm_isd_accept_commit(d["logits"], d["qo1"], d["mode"], d["drafts"], d["dq"],
+                                 st.logits0, d["prow"], w.N, w.temperature, L.PROPOSE_ARGMAX, 0,
+                                 base + k, o["n_accepted"], o["out_tokens"], o["n_out"],
+                                 o["n_commit"], o["next_drafts"], o["next_q_stats"],
+                                 o["next_mode"], o["next_mask_row0"], st.k_cache, st.v_cache,
+                                 d["page_table"], d["seq_lens"], seq_out, d["k_new"], d["v_new"],
+                                 st.acc_ws, st.status, releasable_from=st.releasable)
 
     rate = None
     for rep in range(2):   # one untimed pass, then the timed one
@@ -801,23 +845,20 @@ def workload_leg(name, dev, steps=20):
     outs = [st.outs() for _ in range(steps)]
     for i in range(3):
         st.attention()
-        st.accept(outs[0], 40_000_000 + i)
-        st.commit(outs[0])
+        st.tail(outs[0], 40_000_000 + i)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     for k in range(steps):
         ev[k][0].record()
         st.attention()
         ev[k][1].record()
-        st.accept(outs[k], k + 1)
+        st.accept_commit(outs[k], k + 1)
         ev[k][2].record()
-        st.commit(outs[k])
         ev[k][3].record()
     torch.cuda.synchronize()
     assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
     att = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     acc = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
-    com = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
     tot = sum(e[0].elapsed_time(e[3]) for e in ev) / steps
     n_out = torch.stack([o["n_out"] for o in outs]).sum().item()
     n_rej = torch.stack([(o["next_mode"] == 0).sum() for o in outs]).sum().item()
@@ -831,8 +872,8 @@ def workload_leg(name, dev, steps=20):
            "attention": {"us": att * 1e3, "GB/s": ab / (att * 1e-3) / 1e9,
                          "frac": ab / (att * 1e-3) / 1e9 / hbm, "algorithmic_bytes": ab},
            "accept": {"us": acc * 1e3, "GB/s": cb / (acc * 1e-3) / 1e9,
-                      "frac": cb / (acc * 1e-3) / 1e9 / hbm, "algorithmic_bytes": cb},
-           "commit": {"us": com * 1e3}}
+                      "frac": cb / (acc * 1e-3) / 1e9 / hbm, "algorithmic_bytes": cb,
+                      "includes_kv_commit": True}}
     del st, outs
     torch.cuda.empty_cache()
     return res

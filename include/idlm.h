@@ -264,6 +264,38 @@ idlm_status idlm_isd_accept(
     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Accept + KV commit in one call ([IDLM] "Inference & ISD" and "Serving
+ * (SGLang)": the kept rows of a step go to the paged KV cache).
+ *
+ * The same outputs as idlm_isd_accept followed by idlm_kv_commit with
+ * n_commit from the accept (the cache, seq_lens_out and releasable_from as
+ * idlm_kv_commit writes them).  The accept's decision kernel appends each
+ * request's commit to its residual kernel's work list, so the copies run
+ * beside the residual and draw work and the call launches the accept's three
+ * kernels and nothing else.
+ *   logits .. dbg    as for idlm_isd_accept
+ *   k_cache .. releasable_from, Hkv, D, page_size, num_pages, kv_dtype
+ *                    as for idlm_kv_commit (k_new / v_new: the step's new
+ *                    keys and values, rows as qo_indptr lays them out)
+ *   workspace        idlm_isd_accept_workspace_size(C, T, N, V) bytes
+ * Device errors: those of both calls.
+ * ---------------------------------------------------------------------- */
+idlm_status idlm_isd_accept_commit(
+    const void* logits, int dtype, int V, const int32_t* qo_indptr,
+    const uint8_t* mode, const int32_t* drafts, const float* draft_q_stats,
+    const void* prev_logits, int prev_rows, const int32_t* prev_mask_row0,
+    int C, int T, int N, float temperature, int proposal_mode,
+    uint64_t seed, uint64_t step,
+    int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out, int32_t* n_commit,
+    int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+    int32_t* next_mask_row0, float* row_stats, float* dbg,
+    void* k_cache, void* v_cache, const int32_t* page_table, int max_pages,
+    const int32_t* seq_lens_in, int32_t* seq_lens_out, const void* k_new,
+    const void* v_new, int Hkv, int D, int page_size, int num_pages, int kv_dtype,
+    int32_t* releasable_from, void* workspace, size_t workspace_bytes,
+    int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused LM head + accept ([IDLM] "Inference & ISD": p and q both come from
  * the one forward pass, whose last product is the LM head).
  *

@@ -100,6 +100,12 @@ def lib():
         L.idlm_kv_commit.restype = i32
         L.idlm_kv_commit.argtypes = ([vp, vp, vp, i32, vp, vp, vp, vp, vp, vp] + [i32] * 7
                                      + [vp, vp, vp])
+        L.idlm_isd_accept_commit.restype = i32
+        L.idlm_isd_accept_commit.argtypes = (
+            [vp, i32, i32] + [vp] * 5 + [i32, vp] + [i32, i32, i32, f32, i32, u64, u64]
+            + [vp] * 10
+            + [vp, vp, vp, i32, vp, vp, vp, vp] + [i32] * 5 + [vp]
+            + [vp, sz, vp, vp])
         _lib = L
     return _lib
 
@@ -290,6 +296,35 @@ def idlm_kv_commit(k_cache, v_cache, page_table, seq_lens_in, seq_lens_out, k_ne
         D, page_size, num_pages, _dtype(k_cache), _ptr(releasable_from), _ptr(status),
         _stream(stream))
     _check(rc, "idlm_kv_commit")
+
+
+def idlm_isd_accept_commit(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits,
+                           prev_mask_row0, N, temperature, proposal_mode, seed, step,
+                           n_accepted, out_tokens, n_out, n_commit, next_drafts, next_q_stats,
+                           next_mode, next_mask_row0, k_cache, v_cache, page_table, seq_lens_in,
+                           seq_lens_out, k_new, v_new, workspace, status, row_stats=None,
+                           dbg=None, releasable_from=None, stream=None):
+    """idlm_isd_accept, then the KV commit of the kept rows, in one call (the
+    commits run as work items of the accept's residual kernel)."""
+    _contig(logits, qo_indptr, mode, drafts, draft_q_stats, prev_logits, prev_mask_row0,
+            n_accepted, out_tokens, n_out, n_commit, next_drafts, next_q_stats, next_mode,
+            next_mask_row0, workspace, row_stats, dbg, k_cache, v_cache, page_table,
+            seq_lens_in, seq_lens_out, k_new, v_new, releasable_from)
+    T, V = logits.shape
+    C = mode.shape[0]
+    num_pages, Hkv, page_size, D = k_cache.shape
+    max_pages = page_table.shape[1]
+    rc = lib().idlm_isd_accept_commit(
+        _ptr(logits), _dtype(logits), V, _ptr(qo_indptr), _ptr(mode), _ptr(drafts),
+        _ptr(draft_q_stats), _ptr(prev_logits), prev_logits.shape[0], _ptr(prev_mask_row0),
+        C, T, N, float(temperature), int(proposal_mode), int(seed), int(step), _ptr(n_accepted),
+        _ptr(out_tokens), _ptr(n_out), _ptr(n_commit), _ptr(next_drafts), _ptr(next_q_stats),
+        _ptr(next_mode), _ptr(next_mask_row0), _ptr(row_stats), _ptr(dbg), _ptr(k_cache),
+        _ptr(v_cache), _ptr(page_table), max_pages, _ptr(seq_lens_in), _ptr(seq_lens_out),
+        _ptr(k_new), _ptr(v_new), Hkv, D, page_size, num_pages, _dtype(k_cache),
+        _ptr(releasable_from), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _check(rc, "idlm_isd_accept_commit")
 
 
 # ------------------------------------------------------- multi-step loop pieces

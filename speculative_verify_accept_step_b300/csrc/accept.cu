@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "commit.cuh"
 #include "common.cuh"
 #include "host_util.h"
 #include "philox.cuh"
@@ -90,7 +91,8 @@ struct __align__(16) PreRecord {
 
 // One unit of the work kernel, written by the decide kernel.
 struct __align__(16) WorkItem {
-  int c, kind, idx, n_acc;   // kind 0: residual slice idx; kind 1: softmax draw t = idx
+  int c, kind, idx, n_acc;   // kind 0: residual slice idx; kind 1: softmax draw t = idx;
+                             // kind 2: KV commit of idx rows
   int row_x, row_y;          // residual: rows of p_j (this step) and q_j (previous step);
                              // draw: the row drawn from (row_y unused)
   float mx, isx;             // log2-domain max and 1/sum of row x
@@ -129,6 +131,8 @@ struct Params {
   float s2;           // log2(e) / T
   int part_given;     // 1: `part` already holds every chunk record (the fused LM head
                       // wrote them); kernel 1 then only gathers the requests' inputs
+  int do_commit;      // 1: each request's KV commit is a work item (fused accept + commit)
+  CommitArgs cm;
 };
 
 template <typename T>
@@ -837,10 +841,22 @@ __global__ void __launch_bounds__(kDThreads) decide_kernel(const Params p) {
   const bool residual = rejected && !p.greedy;
   const int ndraw = (rejected || p.greedy) ? 0 : (p.propose == IDLM_PROPOSE_SAMPLE ? N : 1);
   const int nitems = residual ? p.nslice : ndraw;
+  const int nall = nitems + (p.do_commit ? 1 : 0);
 
-  // work items for the draws left open
-  if (tid == 0 && nitems) base = atomicAdd(p.work_cnt, nitems);
+  // work items for the draws left open (and the request's KV commit)
+  if (tid == 0 && nall) base = atomicAdd(p.work_cnt, nall);
   __syncthreads();
+  if (p.do_commit && tid == 0) {
+    WorkItem it;
+    it.c = c;
+    it.kind = 2;
+    it.idx = L.full ? 1 + n_acc : 1;
+    it.n_acc = n_acc;
+    it.row_x = it.row_y = 0;
+    it.mx = it.isx = it.my = it.isy = it.u = 0.f;
+    it.pad = 0;
+    p.work[base + nitems] = it;
+  }
   if (tid < nitems) {
     WorkItem it;
     it.c = c;
@@ -918,6 +934,11 @@ __global__ void __launch_bounds__(kWThreads) work_kernel(const Params p) {
   for (int i = blockIdx.x; i < count; i += gridDim.x) {
     const WorkItem it = p.work[i];
     const int c = it.c;
+    if (it.kind == 2) {
+      commit_request(p.cm, c, it.idx);
+      __syncthreads();
+      continue;
+    }
     const T* rx = logits + static_cast<size_t>(it.row_x) * V;
     if (it.kind == 1) {
       row_masses<kWThreads>(p, it.row_x, it.mx, sm.mass);
@@ -1065,7 +1086,7 @@ size_t workspace_bytes(int C, int T, int V, int dtype, Params* p, void* base) {
   int32_t* res_cnt = cv.take<int32_t>(C);
   PreRecord* pre = cv.take<PreRecord>(C);
   const int nslice = (CH + kSliceChunks - 1) / kSliceChunks;
-  WorkItem* work = cv.take<WorkItem>(static_cast<size_t>(C) * std::max(nslice, 16));
+  WorkItem* work = cv.take<WorkItem>(static_cast<size_t>(C) * (std::max(nslice, 16) + 1));
   int32_t* work_cnt = cv.take<int32_t>(1);
   if (p) {
     p->part = part;
@@ -1210,6 +1231,7 @@ idlm_status accept_prepare(acc::Params& p, DeviceInfo& dev, const void* logits, 
   p.prev_rows = prev_rows;
   p.s2 = p.greedy ? 1.f : kLog2e / temperature;
   p.part_given = 0;
+  p.do_commit = 0;
   return IDLM_OK;
 }
 
@@ -1237,6 +1259,57 @@ extern "C" idlm_status idlm_isd_accept(
       n_out, n_commit, next_drafts, next_q_stats, next_mode, next_mask_row0, row_stats, dbg,
       workspace, workspace_bytes, status);
   if (rc != IDLM_OK) return rc;
+  return accept_launch(p, dev, dtype, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------- fused accept + commit
+//
+// The accept step and the KV commit of its kept rows in one call: the
+// decision kernel appends one commit item per request to the residual
+// kernel's work list, so the copies run beside the residual and draw items
+// (on CTAs that have no other item) instead of as a kernel after them.
+
+extern "C" idlm_status idlm_isd_accept_commit(
+    const void* logits, int dtype, int V, const int32_t* qo_indptr, const uint8_t* mode,
+    const int32_t* drafts, const float* draft_q_stats, const void* prev_logits, int prev_rows,
+    const int32_t* prev_mask_row0, int C, int T, int N, float temperature, int proposal_mode,
+    uint64_t seed, uint64_t step, int32_t* n_accepted, int32_t* out_tokens, int32_t* n_out,
+    int32_t* n_commit, int32_t* next_drafts, float* next_q_stats, uint8_t* next_mode,
+    int32_t* next_mask_row0, float* row_stats, float* dbg, void* k_cache, void* v_cache,
+    const int32_t* page_table, int max_pages, const int32_t* seq_lens_in,
+    int32_t* seq_lens_out, const void* k_new, const void* v_new, int Hkv, int D,
+    int page_size, int num_pages, int kv_dtype, int32_t* releasable_from, void* workspace,
+    size_t workspace_bytes, int32_t* status, void* stream) {
+  int row_bytes = 0;
+  idlm_status rc = commit_check(k_cache, v_cache, page_table, max_pages, seq_lens_in,
+                                seq_lens_out, k_new, v_new, Hkv, D, page_size, num_pages,
+                                kv_dtype, &row_bytes);
+  if (rc != IDLM_OK) return rc;
+  acc::Params p;
+  DeviceInfo dev;
+  rc = accept_prepare(p, dev, logits, dtype, V, qo_indptr, mode, drafts, draft_q_stats,
+                      prev_logits, prev_rows, prev_mask_row0, C, T, N, temperature,
+                      proposal_mode, seed, step, n_accepted, out_tokens, n_out, n_commit,
+                      next_drafts, next_q_stats, next_mode, next_mask_row0, row_stats, dbg,
+                      workspace, workspace_bytes, status);
+  if (rc != IDLM_OK) return rc;
+  p.do_commit = 1;
+  p.cm.k_cache = static_cast<uint8_t*>(k_cache);
+  p.cm.v_cache = static_cast<uint8_t*>(v_cache);
+  p.cm.page_table = page_table;
+  p.cm.max_pages = max_pages;
+  p.cm.seq_lens_in = seq_lens_in;
+  p.cm.seq_lens_out = seq_lens_out;
+  p.cm.k_new = static_cast<const uint8_t*>(k_new);
+  p.cm.v_new = static_cast<const uint8_t*>(v_new);
+  p.cm.qo_indptr = qo_indptr;
+  p.cm.T = T;
+  p.cm.Hkv = Hkv;
+  p.cm.row_bytes = row_bytes;
+  p.cm.page_size = page_size;
+  p.cm.num_pages = num_pages;
+  p.cm.releasable_from = releasable_from;
+  p.cm.status = status;
   return accept_launch(p, dev, dtype, static_cast<cudaStream_t>(stream));
 }
 

@@ -10,8 +10,9 @@ This module only wires C-ABI calls together and owns their device buffers
       idlm_synth_logits   the seeded stand-in for the model's forward pass
                           (logit rows of this step's layout)
       idlm_isd_attention  the step rows against the paged KV cache (optional)
-      idlm_isd_accept     p/q test, residual / bonus / fresh draw, proposals
-      idlm_kv_commit      anchor + accepted drafts into the cache
+      idlm_isd_accept_commit  p/q test, residual / bonus / fresh draw,
+                          proposals, and the anchor + accepted drafts into the
+                          cache (the commits as work items of the accept)
       idlm_isd_advance    the next step's row layout, counters, history
 
 Accept state is double-buffered: step k reads the outputs of step k-1 and
@@ -129,15 +130,17 @@ class StationaryLoop:
                                  self.page_table, self.seq_lens, self.qo, self.att_out,
                                  self.att_ws, self.status, max_rows=2 * N - 1,
                                  sm_scale=self.sm_scale)
-        L.idlm_isd_accept(logits, self.qo, prev["next_mode"], prev["next_drafts"],
-                          prev["next_q_stats"], prev_logits, prev["next_mask_row0"], N,
-                          self.temperature, self.proposal_mode, self.seed, step0 + k,
-                          cur["n_accepted"], cur["out_tokens"], cur["n_out"], cur["n_commit"],
-                          cur["next_drafts"], cur["next_q_stats"], cur["next_mode"],
-                          cur["next_mask_row0"], self.acc_ws, self.status)
-        L.idlm_kv_commit(self.k_cache, self.v_cache, self.page_table, self.seq_lens,
-                         self.seq_lens, self.k_new, self.v_new, self.qo, cur["n_commit"],
-                         self.status, releasable_from=self.releasable)
+        # accept, then the kept rows into the cache (lengths advanced in place),
+        # in one call
+        L.idlm_isd_accept_commit(logits, self.qo, prev["next_mode"], prev["next_drafts"],
+                                 prev["next_q_stats"], prev_logits, prev["next_mask_row0"], N,
+                                 self.temperature, self.proposal_mode, self.seed, step0 + k,
+                                 cur["n_accepted"], cur["out_tokens"], cur["n_out"],
+                                 cur["n_commit"], cur["next_drafts"], cur["next_q_stats"],
+                                 cur["next_mode"], cur["next_mask_row0"], self.k_cache,
+                                 self.v_cache, self.page_table, self.seq_lens, self.seq_lens,
+                                 self.k_new, self.v_new, self.acc_ws, self.status,
+                                 releasable_from=self.releasable)
         L.idlm_isd_advance(N, prev["next_mode"], cur["next_mode"], cur["out_tokens"],
                            cur["n_out"], cur["n_accepted"], cur["next_drafts"], self.seq_lens,
                            self.qo, self.row_req, self.row_pos, self.row_token, self.status,

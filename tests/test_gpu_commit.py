@@ -69,3 +69,51 @@ def test_commit_errors_write_nothing(cuda_device):
     okc, _, osl, _ = _oracle(dict(a, page_table=a["page_table"]), torch.tensor([2, 0, 2, 2]))
     assert np.array_equal(kc.view(torch.int16).numpy(), okc)
     assert sl[0].item() == osl[0] and sl[2].item() == osl[2]
+
+
+@pytest.mark.parametrize("name", ["isd_c4_n4_ctx512_2048", "isd_c64_n4_ctx4096"])
+def test_fused_accept_commit_equals_accept_then_commit(cuda_device, name):
+    """idlm_isd_accept_commit (the commits as work items of the accept's
+    residual kernel) writes the same accept outputs, cache, lengths and
+    releasable pages, bit for bit, as idlm_isd_accept followed by
+    idlm_kv_commit on the same inputs (whose commit is oracle-checked above)."""
+    from _gpu import alloc_accept, gpu_accept
+    from oracle import isd
+    dev = "cuda"
+    w = wl.WORKLOADS[name]
+    a = wl.attention_inputs(w)
+    b = wl.accept_inputs(w)
+    C, N = w.C, w.N
+    qo1 = b["qo1"].to(dev)
+    assert torch.equal(a["qo_indptr"], b["qo1"])
+    l0, l1 = b["logits0"].to(dev), b["logits1"].to(dev)
+    M = N - 1
+    s0 = gpu_accept(l0, b["qo0"].to(dev), b["mode0"].to(dev),
+                    torch.full((C, M), -1, dtype=torch.int32, device=dev),
+                    torch.zeros((C, M, 2), dtype=torch.float32, device=dev), l0,
+                    torch.zeros(C, dtype=torch.int32, device=dev), N, 1.0, isd.PROPOSE_ARGMAX, 0, 0)
+    args = (qo1, s0["next_mode"], s0["next_drafts"], s0["next_q_stats"], l0, s0["next_mask_row0"],
+            N, 1.0, isd.PROPOSE_ARGMAX, 0, 1)
+    ref = gpu_accept(l1, *args)
+    kc_ref, vc_ref, sl_ref, rel_ref, st_ref = _run(a, ref["n_commit"].cpu())
+    assert st_ref == 0
+    T, V = l1.shape
+    o = alloc_accept(C, N, T, dev)
+    ws = torch.empty(lib.idlm_isd_accept_workspace_size(C, T, N, V), dtype=torch.uint8, device=dev)
+    kc, vc = a["k_cache"].to(dev), a["v_cache"].to(dev)
+    sl_in = a["seq_lens"].to(dev)
+    sl_out = torch.full_like(sl_in, -1)
+    rel = torch.full_like(sl_in, -1)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.idlm_isd_accept_commit(l1, *args, o["n_accepted"], o["out_tokens"], o["n_out"],
+                               o["n_commit"], o["next_drafts"], o["next_q_stats"], o["next_mode"],
+                               o["next_mask_row0"], kc, vc, a["page_table"].to(dev), sl_in, sl_out,
+                               a["k_new"].to(dev), a["v_new"].to(dev), ws, st,
+                               row_stats=o["row_stats"], dbg=o["dbg"], releasable_from=rel)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for k in ("n_accepted", "out_tokens", "n_out", "n_commit", "next_drafts", "next_q_stats",
+              "next_mode", "next_mask_row0", "row_stats"):
+        assert torch.equal(o[k], ref[k]), k
+    assert torch.equal(kc.cpu(), kc_ref) and torch.equal(vc.cpu(), vc_ref)
+    assert torch.equal(sl_out.cpu(), sl_ref) and torch.equal(rel.cpu(), rel_ref)
