@@ -424,6 +424,10 @@ __global__ void __launch_bounds__(kK1Threads, 1) vocab_stream_kernel(const Param
     fence_barrier_init();
   }
   __syncthreads();
+  // launched as a programmatic dependent of the kernel before it: its
+  // results (the logits, the previous step's state) are read only after it
+  // has finished
+  griddep_wait();
   griddep_launch_dependents();
 
   // rows in use: qo_indptr[C] (T is the capacity of the logits buffer, so a
@@ -1127,20 +1131,27 @@ idlm_status launch(const Params& p, int dev, int sm_count, cudaStream_t stream) 
   }
   const long long W = static_cast<long long>(p.T) * p.CH;
   const int grid1 = static_cast<int>(std::min<long long>(sm_count, W));
-  vocab_stream_kernel<T><<<grid1, kK1Threads, kK1Smem, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return IDLM_ERR_CUDA;
-
-  // the decide and work kernels start early as programmatic dependents and
-  // wait in griddepcontrol.wait for the results of the kernel before them
+  // all three kernels start early as programmatic dependents and wait in
+  // griddepcontrol.wait for the results of the kernel before them
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+  cfg.gridDim = dim3(grid1);
+  cfg.blockDim = dim3(kK1Threads);
+  cfg.dynamicSmemBytes = kK1Smem;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, vocab_stream_kernel<T>, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, vocab_stream_kernel<T>, p);
+    cfg.numAttrs = 1;
+  }
+  if (e != cudaSuccess) return IDLM_ERR_CUDA;
+  cfg.dynamicSmemBytes = 0;
   cfg.gridDim = dim3(p.C);
   cfg.blockDim = dim3(kDThreads);
   e = cudaLaunchKernelEx(&cfg, decide_kernel<T>, p);
