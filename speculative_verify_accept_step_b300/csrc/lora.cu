@@ -44,6 +44,10 @@
 // a segment of a left-over tile that a CTA does not hold whole is written as
 // an fp32 partial tile and summed by the fix-up kernel.  No CTA waits for
 // another, and the sums do not depend on timing.
+// For the LM head of the fused LM-head + accept call (no adapter, Y = the
+// logits) the epilogue and the fix-up also write the softmax statistics of
+// every token row over each 128-entry tile (TileStat), read back from the
+// bf16 values they store.
 // Every mbarrier wait is bounded; a wait that runs out records
 // IDLM_DEV_TIMEOUT, and the CTA drains its copies and MMAs and frees its
 // tensor memory before it leaves.
