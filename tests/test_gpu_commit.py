@@ -117,3 +117,83 @@ def test_fused_accept_commit_equals_accept_then_commit(cuda_device, name):
         assert torch.equal(o[k], ref[k]), k
     assert torch.equal(kc.cpu(), kc_ref) and torch.equal(vc.cpu(), vc_ref)
     assert torch.equal(sl_out.cpu(), sl_ref) and torch.equal(rel.cpu(), rel_ref)
+
+
+def _fused_call(a, b_logits, qo, mode, drafts, dq, prev, prow, N, step, page_table=None,
+                dev="cuda"):
+    from _gpu import alloc_accept
+    from oracle import isd
+    C = mode.shape[0]
+    T, V = b_logits.shape
+    o = alloc_accept(C, N, T, dev)
+    ws = torch.empty(lib.idlm_isd_accept_workspace_size(C, T, N, V), dtype=torch.uint8, device=dev)
+    kc, vc = a["k_cache"].to(dev), a["v_cache"].to(dev)
+    sl_in = a["seq_lens"].to(dev)
+    sl_out = torch.full_like(sl_in, -1)
+    rel = torch.full_like(sl_in, -1)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pt = (a["page_table"] if page_table is None else page_table).to(dev)
+    lib.idlm_isd_accept_commit(b_logits, qo, mode, drafts, dq, prev, prow, N, 1.0,
+                               isd.PROPOSE_ARGMAX, 0, step, o["n_accepted"], o["out_tokens"],
+                               o["n_out"], o["n_commit"], o["next_drafts"], o["next_q_stats"],
+                               o["next_mode"], o["next_mask_row0"], kc, vc, pt, sl_in, sl_out,
+                               a["k_new"].to(dev), a["v_new"].to(dev), ws, st,
+                               row_stats=o["row_stats"], dbg=o["dbg"], releasable_from=rel)
+    torch.cuda.synchronize()
+    return o, kc.cpu(), vc.cpu(), sl_out.cpu(), rel.cpu(), int(st.item())
+
+
+def test_fused_accept_commit_fresh_step(cuda_device):
+    """A FRESH step through the fused call: every request commits its one
+    clean row (n_commit = 1), bit for bit as idlm_kv_commit does."""
+    from _gpu import gpu_accept
+    from oracle import isd
+    dev = "cuda"
+    w = wl.WORKLOADS["isd_c4_n4_ctx512_2048"]
+    b = wl.accept_inputs(w)
+    C, N = w.C, w.N
+    M = N - 1
+    # a FRESH step's rows (N per request) with the cache inputs of the same shape
+    a = wl.attention_inputs(w, mode=torch.zeros(C, dtype=torch.int64))
+    assert torch.equal(a["qo_indptr"], b["qo0"])
+    l0 = b["logits0"].to(dev)
+    qo0 = b["qo0"].to(dev)
+    args = (qo0, b["mode0"].to(dev), torch.full((C, M), -1, dtype=torch.int32, device=dev),
+            torch.zeros((C, M, 2), dtype=torch.float32, device=dev), l0,
+            torch.zeros(C, dtype=torch.int32, device=dev))
+    ref = gpu_accept(l0, *args, N, 1.0, isd.PROPOSE_ARGMAX, 0, 0)
+    assert torch.all(ref["n_commit"] == 1)
+    kc_ref, vc_ref, sl_ref, rel_ref, st_ref = _run(a, ref["n_commit"].cpu())
+    o, kc, vc, sl, rel, st = _fused_call(a, l0, *args, N, 0)
+    assert st == 0 and st_ref == 0
+    for k in ("n_accepted", "out_tokens", "n_commit", "next_drafts", "next_mode"):
+        assert torch.equal(o[k], ref[k]), k
+    assert torch.equal(kc, kc_ref) and torch.equal(vc, vc_ref)
+    assert torch.equal(sl, sl_ref) and torch.equal(rel, rel_ref)
+
+
+def test_fused_accept_commit_bad_page_writes_nothing_for_that_request(cuda_device):
+    """A page id outside the pool on the slot a request would write: the
+    fused call sets BAD_PAGE and leaves that request's cache rows and length
+    untouched, while the other requests commit."""
+    from oracle import isd
+    dev = "cuda"
+    w = wl.WORKLOADS["isd_c4_n4_ctx512_2048"]
+    b = wl.accept_inputs(w)
+    C, N = w.C, w.N
+    M = N - 1
+    a = wl.attention_inputs(w, mode=torch.zeros(C, dtype=torch.int64))
+    L1 = int(a["seq_lens"][1])
+    pt = a["page_table"].clone()
+    pt[1, L1 // 16] = 999_999
+    l0 = b["logits0"].to(dev)
+    args = (b["qo0"].to(dev), b["mode0"].to(dev),
+            torch.full((C, M), -1, dtype=torch.int32, device=dev),
+            torch.zeros((C, M, 2), dtype=torch.float32, device=dev), l0,
+            torch.zeros(C, dtype=torch.int32, device=dev))
+    o, kc, vc, sl, rel, st = _fused_call(a, l0, *args, N, 0, page_table=pt)
+    assert st == 1   # BAD_PAGE
+    assert sl[1].item() == -1 and rel[1].item() == -1
+    okc, _, osl, _ = _oracle(dict(a, page_table=pt), torch.tensor([1, 0, 1, 1]))
+    assert np.array_equal(kc.view(torch.int16).numpy(), okc)
+    assert sl[0].item() == osl[0] and sl[2].item() == osl[2] and sl[3].item() == osl[3]
