@@ -297,6 +297,9 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
     const int R = min(min(max(p.qo_indptr[c + 1] - t0, 0), p.max_rows), p.T - t0);
     const bool va = r_a < R, vb = r_b < R;
     const int nbc = cur.nbc, nb = cur.nb;
+    // The unit stays the same within a segment, so the loop below counts
+    // only the block within it and moves the cursor once, at the end.
+    int kb = cur.k;
 
     // Q fragments of this m-tile (rows past R are zero)
     uint32_t qa[8][4];
@@ -328,10 +331,9 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
       const bool two = ((i & 1) == 0) && (j + 1 < seg_end);
       const int nblk = two ? 2 : 1;
       if (((i >> 1) & 1) != par) {
-        advance(cur, p, pref, C, p.Hkv);
-        if (two) advance(cur, p, pref, C, p.Hkv);
         j += nblk;
         i += nblk;
+        kb += nblk;
         continue;
       }
       const int s0 = i % STAGES;
@@ -370,7 +372,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
         // 8n + qc + e within its block.
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
-          const int k = cur.k + bb;
+          const int k = kb + bb;
           if (bb == 1 && !two) {
 #pragma unroll
             for (int n = 2; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = kNegInf;
@@ -471,11 +473,13 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
         if (!released) mbar_arrive(&empty[s0]);
         if (two) mbar_arrive(&empty[s0 + 1]);
       }
-      advance(cur, p, pref, C, p.Hkv);
-      if (two) advance(cur, p, pref, C, p.Hkv);
       j += nblk;
       i += nblk;
+      kb += nblk;
     }
+    // on to the next unit's first block
+    cur.k = nb - 1;
+    advance(cur, p, pref, C, p.Hkv);
 
     // ---- end of this unit's segment: merge the two parity halves
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
