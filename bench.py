@@ -30,9 +30,10 @@ import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "ISD accepted tokens/s at C=64,N=4; attention+accept HBM GB/s vs B300 peak"
-# library launches per timed step: attention 1, accept 3 (the KV commit runs
-# as work items of the accept's residual kernel); 5 with --separate-commit
-LAUNCHES_PER_STEP = 4
+# library kernel launches per timed step: attention 2 (the pass and the merge
+# of units cut between CTAs), accept 3 (the KV commit runs as work items of
+# the accept's residual kernel); 6 with --separate-commit
+LAUNCHES_PER_STEP = 5
 
 
 def parse():
@@ -50,8 +51,8 @@ def parse():
                     help="skip the ragged 1k-32k workload leg")
     ap.add_argument("--no-lmhead", action="store_true", help="skip the fused LM-head leg")
     ap.add_argument("--separate-commit", action="store_true",
-                    help="time the step as idlm_isd_accept then idlm_kv_commit (5 launches) "
-                         "instead of idlm_isd_accept_commit (4)")
+                    help="time the step as idlm_isd_accept then idlm_kv_commit (6 launches) "
+                         "instead of idlm_isd_accept_commit (5)")
     ap.add_argument("--leg", default="step", choices=["step", "lora", "layer", "loop", "lmhead"],
                     help="lora: only the gated-LoRA projections (prints their JSON)")
     ap.add_argument("--lora-reps", type=int, default=20)
@@ -345,8 +346,8 @@ def loop_leg(dev, steps=200, warm=10, target=0.9):
             "model_ms_per_step": model_ms,
             "tokens_per_s_without_model": d["tokens"] / ((ms - model_ms * steps) * 1e-3),
             # synth, attention, accept + commit, advance; kernels: synth 1,
-            # attention 1, accept 3 (the commit as its work items), advance 1
-            "api_calls_per_step": 4, "kernel_launches_per_step": 6,
+            # attention 2, accept 3 (the commit as its work items), advance 1
+            "api_calls_per_step": 4, "kernel_launches_per_step": 7,
             "note": "ms_per_step includes the synthetic model kernel (the step's logits, one "
                     "Philox4x32-10 per logit); model_ms_per_step is that kernel timed alone"}
 
@@ -728,7 +729,8 @@ def run_ours(args):
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "inputs larger than L2 (KV %.2f GB + logits %.0f MB read per step)"
                          % (a_bytes / 1e9, w.T * w.V * 2 / 1e6)},
-        "roofline": {"bound": "hbm", "kernel": "paged_attn_kernel (idlm_isd_attention)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "idlm_isd_attention (paged_attn_kernel + attn_merge_kernel)",
                      "achieved": att_gbs, "peak": hbm, "unit": "GB/s", "frac": att_gbs / hbm,
                      "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes": a_bytes},
@@ -743,9 +745,9 @@ def run_ours(args):
         "tokens_per_step": n_out / K,
         "accepted_drafts_per_step": n_acc / K,
         "accepted_drafts_per_s": allreduce(float(n_acc), ws, _sum_op()) / (ms * 1e-3),
-        # per step: paged_attn_kernel; vocab_stream_kernel, decide_kernel,
-        # work_kernel (which also commits the KV rows); commit_kernel only with
-        # --separate-commit (no memsets or copies)
+        # per step: paged_attn_kernel, attn_merge_kernel; vocab_stream_kernel,
+        # decide_kernel, work_kernel (which also commits the KV rows);
+        # commit_kernel only with --separate-commit (no memsets or copies)
         "gpu_launches": (LAUNCHES_PER_STEP + (0 if fused else 1)) * K,
         "clocks": clk,
         "e2e": e2e,

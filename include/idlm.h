@@ -110,7 +110,9 @@ const char* idlm_status_string(int status);
  *   dtype      IDLM_BF16 or IDLM_F32 for q, k_*, v_*, caches and out
  *   max_rows   upper bound on qo_indptr[c+1]-qo_indptr[c] (e.g. 2N-1)
  * Fast path: dtype BF16, D = 128, page_size = 16, (Hq/Hkv) * max_rows <= 64
- * (a TMA-fed tensor-core kernel); other shapes run a simple CUDA-core kernel
+ * (a TMA-fed tensor-core kernel, then a small kernel that merges the KV
+ * ranges of a (request, KV head) split between CTAs, launched as its
+ * programmatic dependent); other shapes run a simple CUDA-core kernel
  * (any page_size, D a multiple of 32 up to 256).  Device errors: BAD_PAGE,
  * BAD_LAYOUT (a request with more than max_rows rows), TIMEOUT.
  * Workspace: idlm_isd_attention_workspace_size(); it depends on the current

@@ -15,8 +15,10 @@
 // blocks of the step's own new rows); a persistent grid splits that list evenly
 // (balanced split-KV), so long and short contexts load the SMs equally.
 // Units cut by a CTA boundary write partial (max, sum, O) triples to the
-// workspace and the last CTA to finish a unit (atomic arrival count, no
-// waiting) merges them.
+// workspace, and a small second kernel, launched as a programmatic dependent,
+// merges them once the grid is done: no CTA waits for another, no counter
+// or fence sits at the end of a CTA's range, and the sums do not depend on
+// timing.
 //
 // Per CTA: one producer warp issues TMA tile loads (cp.async.bulk.tensor,
 // 128-byte swizzle) into an 8-stage shared-memory ring guarded by mbarriers:
@@ -31,8 +33,6 @@
 // The general path (fp32, or any other D / page size) is a plain kernel with
 // one warp per (row, head) walking the keys in order.
 #include <algorithm>
-#include <atomic>
-#include <chrono>
 
 #include "common.cuh"
 #include "host_util.h"
@@ -61,10 +61,8 @@ struct Params {
   const int32_t* page_table;
   const int32_t* seq_lens;
   const int32_t* qo_indptr;
-  float* ws_o;       // [B][2][MT*16][D]
-  float* ws_ml;      // [B][2][MT*16][2]
-  unsigned long long* ws_cnt;   // [C*Hkv]: launch epoch << 32 | parts merged
-  unsigned long long epoch;     // distinct for every launch (low 32 bits used)
+  float* ws_o;       // [B][2][MT*16][D]: partial O of a cut unit's part
+  float* ws_ml;      // [B][2][MT*16][2]: its (max, sum) per row
   int32_t* status;
   int max_pages, C, T, Hq, Hkv, G, num_pages, max_rows;
   float scale_log2;  // sm_scale * log2(e)
@@ -133,6 +131,53 @@ __device__ __forceinline__ void advance(Cursor& cur, const Params& p, const int*
   cur.nbc = cached_blocks(p, cur.c);
 }
 
+// pref[c] = blocks of requests 0 .. c-1: ceil(L / 16) cached pages plus
+// ceil(R / 16) blocks of new rows (at least one, so that every unit has a
+// block).  Every thread of the CTA calls it; a barrier must follow before
+// pref is read.  With check set, bad layouts and lengths go to the status.
+template <int NT>
+__device__ __forceinline__ void block_prefix(const Params& p, int* pref, bool check) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int C = p.C;
+  const int per = (C + NT - 1) / NT;
+  const int c0 = min(C, tid * per), c1 = min(C, c0 + per);
+  int sum = 0;
+  for (int c = c0; c < c1; ++c) {
+    int L = p.seq_lens[c];
+    const int rows = p.qo_indptr[c + 1] - p.qo_indptr[c];
+    if (check) {
+      if (L < 0 || rows < 0 || rows > p.max_rows || p.qo_indptr[c] < 0 ||
+          p.qo_indptr[c + 1] > p.T)
+        set_status(p.status, IDLM_DEV_BAD_LAYOUT);
+      if (L > p.max_pages * PS) set_status(p.status, IDLM_DEV_SLOT_OVERFLOW);
+    }
+    L = min(max(L, 0), p.max_pages * PS);
+    const int R = min(max(rows, 0), p.max_rows);
+    pref[c + 1] = (L + PS - 1) / PS + max(1, (R + PS - 1) / PS);   // temporarily the count
+    sum += pref[c + 1];
+  }
+  // exclusive scan of the per-thread sums: shuffles within a warp, then the
+  // warp totals
+  __shared__ int wsum[NT / 32];
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  if (tid == 0) pref[0] = 0;
+  __syncthreads();
+  int acc = incl - sum;
+  for (int w = 0; w < warp; ++w) acc += wsum[w];
+  for (int c = c0; c < c1; ++c) {
+    acc += pref[c + 1];
+    pref[c + 1] = acc;
+  }
+}
+
 __device__ __forceinline__ long long range_lo(long long W, int B, int b) {
   return W * b / B;
 }
@@ -175,41 +220,7 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
     }
     fence_barrier_init();
   }
-  {
-    const int per = (C + LY::kThreads - 1) / LY::kThreads;
-    const int c0 = min(C, tid * per), c1 = min(C, c0 + per);
-    int sum = 0;
-    for (int c = c0; c < c1; ++c) {
-      int L = p.seq_lens[c];
-      const int rows = p.qo_indptr[c + 1] - p.qo_indptr[c];
-      if (L < 0 || rows < 0 || rows > p.max_rows || p.qo_indptr[c] < 0 ||
-          p.qo_indptr[c + 1] > p.T)
-        set_status(p.status, IDLM_DEV_BAD_LAYOUT);
-      if (L > p.max_pages * PS) set_status(p.status, IDLM_DEV_SLOT_OVERFLOW);
-      L = min(max(L, 0), p.max_pages * PS);
-      const int R = min(max(rows, 0), p.max_rows);
-      pref[c + 1] = (L + PS - 1) / PS + max(1, (R + PS - 1) / PS);   // temporarily the count
-      sum += pref[c + 1];
-    }
-    // exclusive scan of the per-thread sums: shuffles within a warp, then
-    // the warp totals
-    __shared__ int wsum[LY::kThreads / 32];
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    if (tid == 0) pref[0] = 0;
-    __syncthreads();
-    int acc = incl - sum;
-    for (int w = 0; w < warp; ++w) acc += wsum[w];
-    for (int c = c0; c < c1; ++c) {
-      acc += pref[c + 1];
-      pref[c + 1] = acc;
-    }
-  }
+  block_prefix<LY::kThreads>(p, pref, true);
   fence_proxy_async();
   __syncthreads();
 
@@ -542,7 +553,8 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
           if (vb) out_b[(8 * n + qc) >> 1] = pack_bf16x2(o[n][2] * ib, o[n][3] * ib);
         }
       } else {
-        // partial: slot 0 if this segment opened the CTA's range, else slot 1
+        // a part of a unit cut by a CTA boundary: (max, sum, O) for the merge
+        // kernel, in slot 0 if this segment opened the CTA's range, else slot 1
         const int slot = (seg_start == lo) ? 0 : 1;
         const size_t sbase = (static_cast<size_t>(blockIdx.x) * 2 + slot) * (MT * 16);
         float* wo = p.ws_o + sbase * D;
@@ -558,79 +570,101 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
           wml[2 * row_b] = m_b;
           wml[2 * row_b + 1] = l_b;
         }
-        __threadfence();
-        named_bar(1 + MT, 32 * MT);
-        const int u = c * p.Hkv + g;
-        const long long ustart = unit_end - nb;
-        const int bf = owner_of(W, B, ustart);
-        const int bl = owner_of(W, B, unit_end - 1);
-        if (mt == 0 && lane == 0) {
-          // CTAs with an empty range (more CTAs than blocks) hold no part.
-          // The counter carries this launch's epoch in its high half, so a
-          // count left by an interrupted earlier launch reads as zero.
-          int parts = 0;
-          for (int b = bf; b <= bl; ++b) parts += range_lo(W, B, b) < range_lo(W, B, b + 1);
-          const unsigned long long tag = (p.epoch & 0xffffffffull) << 32;
-          unsigned long long* cnt = p.ws_cnt + u;
-          unsigned long long seen, old = *reinterpret_cast<volatile unsigned long long*>(cnt);
-          do {
-            seen = old;
-            const unsigned long long nv =
-                ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
-            old = atomicCAS(cnt, seen, nv);
-          } while (old != seen);
-          const unsigned long long now =
-              ((seen & ~0xffffffffull) == tag) ? seen + 1 : tag + 1;
-          flags[1] = (now & 0xffffffffull) == static_cast<unsigned long long>(parts);
-          // the last part clears the counter: a CUDA graph replays this launch
-          // with the same epoch, and must find the count at zero again
-          if (flags[1]) atomicExch(cnt, 0ull);
-        }
-        named_bar(1 + MT, 32 * MT);
-        const bool last = flags[1] != 0;
-        if (last) {
-          __threadfence();
-          float Ma = kNegInf, Mb = kNegInf;
-          for (int b = bf; b <= bl; ++b) {
-            if (range_lo(W, B, b) >= range_lo(W, B, b + 1)) continue;
-            const int sl = (b == bf && ustart > range_lo(W, B, b)) ? 1 : 0;
-            const size_t pb = (static_cast<size_t>(b) * 2 + sl) * (MT * 16);
-            Ma = fmaxf(Ma, __ldcg(p.ws_ml + (pb + row_a) * 2));
-            Mb = fmaxf(Mb, __ldcg(p.ws_ml + (pb + row_b) * 2));
-          }
-          const float ba = Ma == kNegInf ? 0.f : Ma, bb = Mb == kNegInf ? 0.f : Mb;
-          float La = 0.f, Lb = 0.f;
-#pragma unroll
-          for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-          for (int b = bf; b <= bl; ++b) {
-            if (range_lo(W, B, b) >= range_lo(W, B, b + 1)) continue;
-            const int sl = (b == bf && ustart > range_lo(W, B, b)) ? 1 : 0;
-            const size_t pb = (static_cast<size_t>(b) * 2 + sl) * (MT * 16);
-            const float fa = fast_exp2(__ldcg(p.ws_ml + (pb + row_a) * 2) - ba);
-            const float fb = fast_exp2(__ldcg(p.ws_ml + (pb + row_b) * 2) - bb);
-            La += fa * __ldcg(p.ws_ml + (pb + row_a) * 2 + 1);
-            Lb += fb * __ldcg(p.ws_ml + (pb + row_b) * 2 + 1);
-            const float* po = p.ws_o + pb * D;
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-              const float2 xa = __ldcg(reinterpret_cast<const float2*>(po + row_a * D + 8 * n + qc));
-              const float2 xb = __ldcg(reinterpret_cast<const float2*>(po + row_b * D + 8 * n + qc));
-              o[n][0] += fa * xa.x;
-              o[n][1] += fa * xa.y;
-              o[n][2] += fb * xb.x;
-              o[n][3] += fb * xb.y;
-            }
-          }
-          const float ia = La > 0.f ? 1.f / La : 0.f, ib = Lb > 0.f ? 1.f / Lb : 0.f;
-#pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            if (va) out_a[(8 * n + qc) >> 1] = pack_bf16x2(o[n][0] * ia, o[n][1] * ia);
-            if (vb) out_b[(8 * n + qc) >> 1] = pack_bf16x2(o[n][2] * ib, o[n][3] * ib);
-          }
-        }
         named_bar(1 + MT, 32 * MT);
       }
     }
+  }
+}
+
+// ------------------------------------------------------------ merge of cuts
+// CTA b merges the unit that CTA b of the attention grid opens at the end of
+// its range when that unit goes on into later CTAs (the CTAs bf = b .. bl
+// hold its parts): per (row, 4 columns) item, M = the parts' largest max,
+// then the sum and O weighted by 2^(max - M), added in CTA order, and O /
+// sum.  It is a programmatic dependent of the attention kernel: the block
+// prefix and the unit are found before griddepcontrol.wait, the parts read
+// after it.  (Measured: 256 threads and one CTA per unit beat 128 or 512
+// threads, four CTAs per unit, and an early launch of this grid.)
+constexpr int kMergeThreads = 256;
+constexpr int kMergeRegParts = 4;   // parts held in registers; more go round a loop
+
+template <int MT>
+__global__ void __launch_bounds__(kMergeThreads)
+attn_merge_kernel(const Params p) {
+  extern __shared__ int pref[];
+  block_prefix<kMergeThreads>(p, pref, false);
+  __syncthreads();
+  const int C = p.C, B = gridDim.x, b = blockIdx.x;
+  const long long W = static_cast<long long>(p.Hkv) * pref[C];
+  const long long lo = range_lo(W, B, b), hi = range_lo(W, B, b + 1);
+  bool mine = lo < hi;
+  Cursor cur;
+  if (mine) {
+    cur = locate(p, pref, C, p.Hkv, hi - 1);
+    mine = cur.unit_start >= lo && cur.unit_start + cur.nb > hi;
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  if (!mine) return;
+  const long long ustart = cur.unit_start;
+  const int bl = owner_of(W, B, ustart + cur.nb - 1);
+  const int c = cur.c, g = cur.g, G = p.G;
+  const int t0 = min(max(p.qo_indptr[c], 0), p.T);
+  const int R = min(min(max(p.qo_indptr[c + 1] - t0, 0), p.max_rows), p.T - t0);
+  // the slot of CTA x's part: 1 for the opener when its range began earlier
+  auto part_row = [&](int x) -> size_t {
+    const int sl = (x == b && ustart > lo) ? 1 : 0;
+    return (static_cast<size_t>(x) * 2 + sl) * (MT * 16);
+  };
+  auto has_part = [&](int x) { return range_lo(W, B, x) < range_lo(W, B, x + 1); };
+  constexpr int Q4 = D / 4;
+  for (int item = threadIdx.x; item < G * R * Q4; item += kMergeThreads) {
+    const int m = item / Q4, q4 = item % Q4;
+    float mp[kMergeRegParts], lp[kMergeRegParts];
+    float4 xp[kMergeRegParts];
+    bool ok[kMergeRegParts];
+#pragma unroll
+    for (int k = 0; k < kMergeRegParts; ++k) {
+      ok[k] = b + k <= bl && has_part(b + k);
+      if (ok[k]) {
+        const size_t pr = part_row(b + k) + m;
+        mp[k] = __ldcg(p.ws_ml + pr * 2);
+        lp[k] = __ldcg(p.ws_ml + pr * 2 + 1);
+        xp[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + pr * D) + q4);
+      }
+    }
+    float M = kNegInf;
+#pragma unroll
+    for (int k = 0; k < kMergeRegParts; ++k)
+      if (ok[k]) M = fmaxf(M, mp[k]);
+    for (int x = b + kMergeRegParts; x <= bl; ++x)
+      if (has_part(x)) M = fmaxf(M, __ldcg(p.ws_ml + (part_row(x) + m) * 2));
+    const float base = M == kNegInf ? 0.f : M;
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float mx, float l, float4 x) {
+      const float f = fast_exp2(mx - base);
+      L = fmaf(f, l, L);
+      o.x = fmaf(f, x.x, o.x);
+      o.y = fmaf(f, x.y, o.y);
+      o.z = fmaf(f, x.z, o.z);
+      o.w = fmaf(f, x.w, o.w);
+    };
+#pragma unroll
+    for (int k = 0; k < kMergeRegParts; ++k)
+      if (ok[k]) add(mp[k], lp[k], xp[k]);
+    for (int x = b + kMergeRegParts; x <= bl; ++x) {
+      if (!has_part(x)) continue;
+      const size_t pr = part_row(x) + m;
+      add(__ldcg(p.ws_ml + pr * 2), __ldcg(p.ws_ml + pr * 2 + 1),
+          __ldcg(reinterpret_cast<const float4*>(p.ws_o + pr * D) + q4));
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int r = m / G, h = g * G + m % G;
+    uint2 v;
+    v.x = pack_bf16x2(o.x * inv, o.y * inv);
+    v.y = pack_bf16x2(o.z * inv, o.w * inv);
+    reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(t0 + r) * p.Hq + h) * D)[q4] = v;
   }
 }
 
@@ -726,7 +760,6 @@ size_t workspace_for(int C, int Hkv, int B) {
   Carver cv(nullptr);
   cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * D);
   cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * 2);
-  cv.take<unsigned long long>(static_cast<size_t>(C) * Hkv);
   return cv.used;
 }
 
@@ -766,13 +799,6 @@ idlm_status launch_fast(const DeviceInfo& dev, const void* q, const void* k_new,
   Params p;
   p.ws_o = cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * D);
   p.ws_ml = cv.take<float>(static_cast<size_t>(B) * 2 * MT * 16 * 2);
-  p.ws_cnt = cv.take<unsigned long long>(static_cast<size_t>(C) * Hkv);
-  // launches get distinct epochs, so a fresh workspace needs no clearing;
-  // the last part of a unit clears its counter for graph replays
-  static std::atomic<unsigned long long> epoch_counter{
-      0x2545f4914f6cdd1dull ^
-      static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};
-  p.epoch = ++epoch_counter;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.page_table = page_table;
@@ -806,7 +832,27 @@ idlm_status launch_fast(const DeviceInfo& dev, const void* q, const void* k_new,
     return IDLM_ERR_CUDA;
 
   paged_attn_kernel<MT><<<B, Layout<MT>::kThreads, Layout<MT>::bytes(C), stream>>>(kc, vc, kn, vn, p);
-  return cuda_status(cudaGetLastError());
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(e);
+  // the merge starts as the attention CTAs finish (a programmatic
+  // dependent), or after the whole grid where the stream does not allow it
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(B);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(C + 1) * sizeof(int);
+  e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<MT>, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<MT>, p);
+  }
+  return cuda_status(e);
 }
 
 }  // namespace attn
