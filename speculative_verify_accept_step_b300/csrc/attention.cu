@@ -583,10 +583,13 @@ paged_attn_kernel(const __grid_constant__ CUtensorMap kc_map,
 // then the sum and O weighted by 2^(max - M), added in CTA order, and O /
 // sum.  It is a programmatic dependent of the attention kernel: the block
 // prefix and the unit are found before griddepcontrol.wait, the parts read
-// after it.  (Measured: 256 threads and one CTA per unit beat 128 or 512
-// threads, four CTAs per unit, and an early launch of this grid.)
+// after it.  Each thread issues the loads of four items before using any,
+// so the merge is one round of loads.  (Measured: 256 threads and one CTA
+// per unit beat 128 or 512 threads, four CTAs per unit, and an early launch
+// of this grid.)
 constexpr int kMergeThreads = 256;
-constexpr int kMergeRegParts = 4;   // parts held in registers; more go round a loop
+constexpr int kMergeRegParts = 2;   // parts held in registers; more go round a loop
+constexpr int kMergeItems = 4;
 
 template <int MT>
 __global__ void __launch_bounds__(kMergeThreads)
@@ -618,53 +621,72 @@ attn_merge_kernel(const Params p) {
   };
   auto has_part = [&](int x) { return range_lo(W, B, x) < range_lo(W, B, x + 1); };
   constexpr int Q4 = D / 4;
-  for (int item = threadIdx.x; item < G * R * Q4; item += kMergeThreads) {
-    const int m = item / Q4, q4 = item % Q4;
-    float mp[kMergeRegParts], lp[kMergeRegParts];
-    float4 xp[kMergeRegParts];
-    bool ok[kMergeRegParts];
+  const int n = G * R * Q4;
+  // the first kMergeRegParts parts: whether they exist and their first rows
+  bool okp[kMergeRegParts];
+  size_t rowp[kMergeRegParts];
 #pragma unroll
-    for (int k = 0; k < kMergeRegParts; ++k) {
-      ok[k] = b + k <= bl && has_part(b + k);
-      if (ok[k]) {
-        const size_t pr = part_row(b + k) + m;
-        mp[k] = __ldcg(p.ws_ml + pr * 2);
-        lp[k] = __ldcg(p.ws_ml + pr * 2 + 1);
-        xp[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + pr * D) + q4);
+  for (int k = 0; k < kMergeRegParts; ++k) {
+    okp[k] = b + k <= bl && has_part(b + k);
+    rowp[k] = okp[k] ? part_row(b + k) : 0;
+  }
+  // kMergeItems items per thread at a time: all their loads issued before
+  // any of them is used
+  for (int i0 = threadIdx.x; i0 < n; i0 += kMergeItems * kMergeThreads) {
+    float mp[kMergeItems][kMergeRegParts], lp[kMergeItems][kMergeRegParts];
+    float4 xp[kMergeItems][kMergeRegParts];
+#pragma unroll
+    for (int it = 0; it < kMergeItems; ++it) {
+      const int item = i0 + it * kMergeThreads;
+      const int m = item / Q4, q4 = item % Q4;
+#pragma unroll
+      for (int k = 0; k < kMergeRegParts; ++k) {
+        if (item < n && okp[k]) {
+          const size_t pr = rowp[k] + m;
+          mp[it][k] = __ldcg(p.ws_ml + pr * 2);
+          lp[it][k] = __ldcg(p.ws_ml + pr * 2 + 1);
+          xp[it][k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + pr * D) + q4);
+        }
       }
     }
-    float M = kNegInf;
 #pragma unroll
-    for (int k = 0; k < kMergeRegParts; ++k)
-      if (ok[k]) M = fmaxf(M, mp[k]);
-    for (int x = b + kMergeRegParts; x <= bl; ++x)
-      if (has_part(x)) M = fmaxf(M, __ldcg(p.ws_ml + (part_row(x) + m) * 2));
-    const float base = M == kNegInf ? 0.f : M;
-    float L = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add = [&](float mx, float l, float4 x) {
-      const float f = fast_exp2(mx - base);
-      L = fmaf(f, l, L);
-      o.x = fmaf(f, x.x, o.x);
-      o.y = fmaf(f, x.y, o.y);
-      o.z = fmaf(f, x.z, o.z);
-      o.w = fmaf(f, x.w, o.w);
-    };
+    for (int it = 0; it < kMergeItems; ++it) {
+      const int item = i0 + it * kMergeThreads;
+      if (item >= n) break;
+      const int m = item / Q4, q4 = item % Q4;
+      float M = kNegInf;
 #pragma unroll
-    for (int k = 0; k < kMergeRegParts; ++k)
-      if (ok[k]) add(mp[k], lp[k], xp[k]);
-    for (int x = b + kMergeRegParts; x <= bl; ++x) {
-      if (!has_part(x)) continue;
-      const size_t pr = part_row(x) + m;
-      add(__ldcg(p.ws_ml + pr * 2), __ldcg(p.ws_ml + pr * 2 + 1),
-          __ldcg(reinterpret_cast<const float4*>(p.ws_o + pr * D) + q4));
+      for (int k = 0; k < kMergeRegParts; ++k)
+        if (okp[k]) M = fmaxf(M, mp[it][k]);
+      for (int x = b + kMergeRegParts; x <= bl; ++x)
+        if (has_part(x)) M = fmaxf(M, __ldcg(p.ws_ml + (part_row(x) + m) * 2));
+      const float base = M == kNegInf ? 0.f : M;
+      float L = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      auto add = [&](float mx, float l, float4 x) {
+        const float f = fast_exp2(mx - base);
+        L = fmaf(f, l, L);
+        o.x = fmaf(f, x.x, o.x);
+        o.y = fmaf(f, x.y, o.y);
+        o.z = fmaf(f, x.z, o.z);
+        o.w = fmaf(f, x.w, o.w);
+      };
+#pragma unroll
+      for (int k = 0; k < kMergeRegParts; ++k)
+        if (okp[k]) add(mp[it][k], lp[it][k], xp[it][k]);
+      for (int x = b + kMergeRegParts; x <= bl; ++x) {
+        if (!has_part(x)) continue;
+        const size_t pr = part_row(x) + m;
+        add(__ldcg(p.ws_ml + pr * 2), __ldcg(p.ws_ml + pr * 2 + 1),
+            __ldcg(reinterpret_cast<const float4*>(p.ws_o + pr * D) + q4));
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const int r = m / G, h = g * G + m % G;
+      uint2 v;
+      v.x = pack_bf16x2(o.x * inv, o.y * inv);
+      v.y = pack_bf16x2(o.z * inv, o.w * inv);
+      reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(t0 + r) * p.Hq + h) * D)[q4] = v;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int r = m / G, h = g * G + m % G;
-    uint2 v;
-    v.x = pack_bf16x2(o.x * inv, o.y * inv);
-    v.y = pack_bf16x2(o.z * inv, o.w * inv);
-    reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(t0 + r) * p.Hq + h) * D)[q4] = v;
   }
 }
 
