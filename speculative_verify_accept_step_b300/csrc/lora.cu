@@ -587,41 +587,52 @@ __device__ __forceinline__ int ystage_at(int j, int col) {
 // stores of whole 256-byte rows.  Thread `row` owns weight row tile*128+row.
 __device__ __noinline__ void store_y_direct(const Params& p, uint32_t taddr, int n_base, int row,
                                             int et, __nv_bfloat16* ystage) {
+  // Params fields in registers: read through the reference after every
+  // shared store, they made this loop ten times slower
+  const int m16 = p.m16, M = p.M, N = p.N;
+  const uint8_t* gate = p.rs_gate;
+  const float scale = p.rs_scale;
+  __nv_bfloat16* const y = p.y;
+  const bool yvec = p.yvec;
+  TileStat* const stats = p.stats;
+  const int tiles = p.tiles, greedy = p.greedy;
+  const float s2 = p.s2;
   uint32_t ra[32];
-  for (int c0 = 0; c0 < p.m16; c0 += 32) {
+  for (int c0 = 0; c0 < m16; c0 += 32) {
     tmem_ld32_async(taddr + c0, ra);
     tmem_ld_wait(ra);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+      float f[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) f[j] = row_factor(gate, scale, min(c0 + 16 * h + j, M - 1));
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        ystage[ystage_at(j, row)] = __float2bfloat16_rn(
-            __uint_as_float(ra[16 * h + j]) *
-            row_factor(p.rs_gate, p.rs_scale, min(c0 + 16 * h + j, p.M - 1)));
+        ystage[ystage_at(j, row)] = __float2bfloat16_rn(__uint_as_float(ra[16 * h + j]) * f[j]);
       epi_sync();
-      if (p.stats) {
+      if (stats) {
         // 16 token rows x the tile's 128 entries: 8 lanes per row, 16 entries each
         const int j = et >> 3, q8 = et & 7;
         const int m = c0 + 16 * h + j;
         float x[16];
         load8_bf16(ystage + ystage_at(j, q8 * 16), x);
         load8_bf16(ystage + ystage_at(j, q8 * 16 + 8), x + 8);
-        TileStat* dst = p.stats + static_cast<size_t>(min(m, p.M - 1)) * p.tiles + n_base / kTileN;
-        tile_stat<8, 16>(p.N, p.s2, p.greedy, x, n_base + q8 * 16, m < p.M ? dst : nullptr);
+        TileStat* dst = stats + static_cast<size_t>(min(m, M - 1)) * tiles + n_base / kTileN;
+        tile_stat<8, 16>(N, s2, greedy, x, n_base + q8 * 16, m < M ? dst : nullptr);
       }
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
         const int idx = it * 128 + et;
         const int rr = idx >> 4, c8 = (idx & 15) * 8;
         const int m = c0 + 16 * h + rr, n0 = n_base + c8;
-        if (m < p.M) {
+        if (m < M) {
           const __nv_bfloat16* src = ystage + ystage_at(rr, c8);
-          __nv_bfloat16* out = p.y + static_cast<size_t>(m) * p.N + n0;
-          if (p.yvec && n0 + 8 <= p.N) {
+          __nv_bfloat16* out = y + static_cast<size_t>(m) * N + n0;
+          if (yvec && n0 + 8 <= N) {
             *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
           } else {
             for (int e = 0; e < 8; ++e)
-              if (n0 + e < p.N) out[e] = src[e];
+              if (n0 + e < N) out[e] = src[e];
           }
         }
       }
@@ -634,31 +645,40 @@ __device__ __noinline__ void store_y_direct(const Params& p, uint32_t taddr, int
 // [m16 x 128] bf16 tile is built there and leaves by TMA store.
 __device__ __noinline__ void store_y_tma(const Params& p, uint32_t taddr, int n_base, int row,
                                          int et, __nv_bfloat16* ytile, const CUtensorMap* y_map) {
+  // Params fields in registers (see store_y_direct)
+  const int m16 = p.m16, M = p.M, N = p.N;
+  const uint8_t* gate = p.rs_gate;
+  const float scale = p.rs_scale;
+  TileStat* const stats = p.stats;
+  const int tiles = p.tiles, greedy = p.greedy;
+  const float s2 = p.s2;
   uint32_t ra[32];
-  for (int c0 = 0; c0 < p.m16; c0 += 32) {
+  for (int c0 = 0; c0 < m16; c0 += 32) {
     tmem_ld32_async(taddr + c0, ra);
     tmem_ld_wait(ra);
+    float f[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) f[j] = row_factor(gate, scale, min(c0 + j, M - 1));
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (c0 + j < p.m16)
-        ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(
-            __uint_as_float(ra[j]) * row_factor(p.rs_gate, p.rs_scale, min(c0 + j, p.M - 1)));
+      if (c0 + j < m16)
+        ytile[(c0 + j) * kTileN + row] = __float2bfloat16_rn(__uint_as_float(ra[j]) * f[j]);
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
-  if (p.stats) {
+  if (stats) {
     // every token row x the tile's 128 entries: 8 lanes per row, 16 entries each
-    for (int g0 = 0; g0 < p.m16; g0 += 16) {
+    for (int g0 = 0; g0 < m16; g0 += 16) {
       const int m = g0 + (et >> 3), q8 = et & 7;
       float x[16];
       load8_bf16(ytile + m * kTileN + q8 * 16, x);
       load8_bf16(ytile + m * kTileN + q8 * 16 + 8, x + 8);
-      TileStat* dst = m < p.M ? p.stats + static_cast<size_t>(m) * p.tiles + n_base / kTileN : nullptr;
-      tile_stat<8, 16>(p.N, p.s2, p.greedy, x, n_base + q8 * 16, dst);
+      TileStat* dst = m < M ? stats + static_cast<size_t>(m) * tiles + n_base / kTileN : nullptr;
+      tile_stat<8, 16>(N, s2, greedy, x, n_base + q8 * 16, dst);
     }
   }
   if (et == 0) {
-    for (int rb0 = 0; rb0 < p.m16; rb0 += kYBoxRows) tma_store_2d(y_map, ytile + rb0 * kTileN, n_base, rb0);
+    for (int rb0 = 0; rb0 < m16; rb0 += kYBoxRows) tma_store_2d(y_map, ytile + rb0 * kTileN, n_base, rb0);
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   }
@@ -669,24 +689,25 @@ __device__ __noinline__ void store_y_tma(const Params& p, uint32_t taddr, int n_
 // the CTA's slot, each store instruction a coalesced 2 KB row of float4s.
 // The next 32 columns are loaded from TMEM while this group's stores go out.
 __device__ __noinline__ void store_partial(const Params& p, uint32_t taddr, int row, float4* dst) {
+  const int m16 = p.m16;   // in a register (see store_y_direct)
   uint32_t ra[32], rb[32];
   tmem_ld32_async(taddr, ra);
-  for (int c0 = 0; c0 < p.m16; c0 += 64) {
+  for (int c0 = 0; c0 < m16; c0 += 64) {
     tmem_ld_wait(ra);
-    const bool more = c0 + 32 < p.m16;
+    const bool more = c0 + 32 < m16;
     if (more) tmem_ld32_async(taddr + c0 + 32, rb);
 #pragma unroll
     for (int g = 0; g < 8; ++g)
-      if (c0 + 4 * g < p.m16)
+      if (c0 + 4 * g < m16)
         __stcg(dst + static_cast<size_t>(c0 / 4 + g) * kTileN + row,
                make_float4(__uint_as_float(ra[4 * g]), __uint_as_float(ra[4 * g + 1]),
                            __uint_as_float(ra[4 * g + 2]), __uint_as_float(ra[4 * g + 3])));
     if (!more) break;
     tmem_ld_wait(rb);
-    if (c0 + 64 < p.m16) tmem_ld32_async(taddr + c0 + 64, ra);
+    if (c0 + 64 < m16) tmem_ld32_async(taddr + c0 + 64, ra);
 #pragma unroll
     for (int g = 0; g < 8; ++g)
-      if (c0 + 32 + 4 * g < p.m16)
+      if (c0 + 32 + 4 * g < m16)
         __stcg(dst + static_cast<size_t>((c0 + 32) / 4 + g) * kTileN + row,
                make_float4(__uint_as_float(rb[4 * g]), __uint_as_float(rb[4 * g + 1]),
                            __uint_as_float(rb[4 * g + 2]), __uint_as_float(rb[4 * g + 3])));
