@@ -919,7 +919,10 @@ __device__ __forceinline__ long long fx_begin(const FParams& f, int c) {
   return static_cast<long long>(c) * f.U_sk / f.G;
 }
 
-__global__ void __launch_bounds__(128) lora_fixup_kernel(const FParams f) {
+constexpr int kFixThreads = 256;   // two threads per weight row, 16 tokens each
+constexpr int kFixBatch = 4;       // parts whose loads are issued before any is added
+
+__global__ void __launch_bounds__(kFixThreads) lora_fixup_kernel(const FParams f) {
   griddep_wait();
   const int chunks = (f.m16 + 31) / 32;
   const int t = blockIdx.x / chunks, ch = blockIdx.x % chunks;
@@ -931,41 +934,59 @@ __global__ void __launch_bounds__(128) lora_fixup_kernel(const FParams f) {
   const int c_last = static_cast<int>((u1 * f.G - 1) / f.U_sk);
   if (c_first == c_last && fx_begin(f, c_first) <= u0 && fx_begin(f, c_first + 1) >= u1)
     return;   // one CTA held the tile whole and wrote its Y
-  const int row = threadIdx.x;
+  const int row = threadIdx.x % kTileN, half = threadIdx.x / kTileN;
   const int nq = f.m16 / 4;
-  float v[32];
+  // this thread's 16 tokens: float4 groups half * 4 .. half * 4 + 3 of the chunk
+  float v[16];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = 0.f;
-  for (int c = c_first; c <= c_last; ++c) {
-    const long long b = fx_begin(f, c), e = fx_begin(f, c + 1);
-    if (b >= e) continue;
-    const int slot = (c == c_first && b < u0) ? 1 : 0;
-    const float4* src = f.part + (static_cast<size_t>(c) * 2 + slot) * nq * kTileN;
+  for (int j = 0; j < 16; ++j) v[j] = 0.f;
+  for (int c0 = c_first; c0 <= c_last; c0 += kFixBatch) {
+    // the loads of up to kFixBatch parts in flight together, then added in
+    // CTA order (the order of K)
+    float4 u[kFixBatch][4];
+    bool has[kFixBatch];
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int col4 = ch * 8 + g;
-      if (col4 < nq) {
-        const float4 u = __ldcg(src + static_cast<size_t>(col4) * kTileN + row);
-        v[4 * g] += u.x;
-        v[4 * g + 1] += u.y;
-        v[4 * g + 2] += u.z;
-        v[4 * g + 3] += u.w;
+    for (int k = 0; k < kFixBatch; ++k) {
+      const int c = c0 + k;
+      const long long b = fx_begin(f, c), e = fx_begin(f, c + 1);
+      has[k] = c <= c_last && b < e;
+      if (has[k]) {
+        const int slot = (c == c_first && b < u0) ? 1 : 0;
+        const float4* src = f.part + (static_cast<size_t>(c) * 2 + slot) * nq * kTileN;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int col4 = ch * 8 + half * 4 + g;
+          u[k][g] = col4 < nq ? __ldcg(src + static_cast<size_t>(col4) * kTileN + row)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kFixBatch; ++k) {
+      if (!has[k]) continue;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        v[4 * g] += u[k][g].x;
+        v[4 * g + 1] += u[k][g].y;
+        v[4 * g + 2] += u[k][g].z;
+        v[4 * g + 3] += u[k][g].w;
       }
     }
   }
   const int n = t * kTileN + row;
   __shared__ __nv_bfloat16 sy[32][kTileN];   // this CTA's 32 token rows of the tile
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int m = ch * 32 + j;
+  for (int jj = 0; jj < 16; ++jj) {
+    const int j = half * 16 + jj, m = ch * 32 + j;
     const __nv_bfloat16 yv =
-        __float2bfloat16_rn(m < f.M ? v[j] * row_factor(f.rs_gate, f.rs_scale, m) : 0.f);
+        __float2bfloat16_rn(m < f.M ? v[jj] * row_factor(f.rs_gate, f.rs_scale, m) : 0.f);
     sy[j][row] = yv;
     if (m < f.M && n < f.N) f.y[static_cast<size_t>(m) * f.N + n] = yv;
   }
   if (f.stats) {
     // 32 token rows x the tile's 128 entries: 4 lanes per row, 32 entries each
     __syncthreads();
+    if (half) return;
     const int j = row >> 2, q4 = row & 3, m = ch * 32 + j;
     float x[32];
 #pragma unroll
@@ -1187,7 +1208,7 @@ idlm_status launch_gemm(const GemmArgs& a, const LoraPlan& pl, int stages, size_
     f.tiles = pl.tiles;
     cudaLaunchConfig_t fc = {};
     fc.gridDim = dim3(pl.sk_tiles * ((pl.m16 + 31) / 32));
-    fc.blockDim = dim3(128);
+    fc.blockDim = dim3(lora::kFixThreads);
     fc.stream = stream;
     fc.attrs = at;
     fc.numAttrs = 1;
