@@ -106,6 +106,9 @@ struct Params {
   int group_end[kMaxGroups];   // first tile after group g
   int R64;        // adapter columns per group in T (r rounded up to 64)
   int stages;     // depth of the stage ring
+  int x_ready;    // W and X may be read at once: the kernel before this one
+                  // is the adapter kernel, launched after all earlier work;
+                  // only T and B (its output) wait in griddepcontrol.wait
   int nacc;       // accumulators in TMEM (2 when m16 <= 256)
   int yvec;       // Y rows allow 16-byte stores (N % 8 == 0, aligned base)
   int ytma;       // the last whole tile goes out by TMA store from the ring
@@ -772,8 +775,11 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
     int issued = 0;
     bool ok = true;
     // X, B and T come from the kernels before this one in the stream (this
-    // grid may have been launched as a programmatic dependent)
-    griddep_wait();
+    // grid may have been launched as a programmatic dependent); behind the
+    // adapter kernel only B and T need the wait, so the weights and X of the
+    // first stages stream in while that kernel runs
+    bool waited = !p.x_ready;
+    if (waited) griddep_wait();
     SegWalk wk(p, blockIdx.x);
     Seg sg;
     while (ok && wk.next(p, sg)) {
@@ -786,6 +792,10 @@ lora_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constan
           break;
         }
         const bool lora_step = k >= p.kb;   // B and T, written by lora_t_kernel
+        if (lora_step && !waited) {
+          griddep_wait();
+          waited = true;
+        }
         if (lane == 0) {
           uint8_t* st = base + size_t(s) * p.stage_bytes;
           const CUtensorMap* am = lora_step ? &b_map : &w_map;
@@ -1116,6 +1126,7 @@ struct GemmArgs {
   lora::TileStat* stats;    // or null: softmax statistics of Y's rows per tile (LM head)
   float s2;
   int greedy;
+  bool x_ready = false;   // see Params::x_ready
 };
 
 // One GEMM launch over a slice of <= 448 token rows, then the fix-up kernel
@@ -1161,6 +1172,7 @@ idlm_status launch_gemm(const GemmArgs& a, const LoraPlan& pl, int stages, size_
   p.stage_bytes = pl.stage_bytes;
   p.wait_ns = a.test_stall ? 20000000ull : kWaitNs;
   p.test_stall = a.test_stall ? 1 : 0;
+  p.x_ready = a.x_ready ? 1 : 0;
   p.stats = a.stats;
   p.s2 = a.s2;
   p.greedy = a.greedy;
@@ -1379,10 +1391,12 @@ idlm_status gated_lora_impl(const void* x, const void* w, const void* lora_a, co
     }
 
     const int tiles = (N + lora::kTileN - 1) / lora::kTileN;
-    const GemmArgs ga{xs, Ms, K, w, N, r, ngroups, gend_rows, R64, wm, xm1, xm2, bm, tm1, tm2,
+    GemmArgs ga{xs, Ms, K, w, N, r, ngroups, gend_rows, R64, wm, xm1, xm2, bm, tm1, tm2,
                       yb + static_cast<size_t>(m0) * N, reinterpret_cast<float4*>(wsb + wl.part),
                       nullptr, 0.f, test_stall,
                       stats ? stats + static_cast<size_t>(m0) * tiles : nullptr, s2, greedy};
+    // right behind the (plainly launched) adapter kernel, X is complete
+    ga.x_ready = r > 0 && R64 != r;
     const idlm_status rc = launch_gemm(ga, pl, stages, smem, status, stream);
     if (rc != IDLM_OK) return rc;
   }
