@@ -148,9 +148,11 @@ def test_bad_page_id_sets_status(cuda_device):
 
 
 def test_graph_replays_merge_split_units(cuda_device):
-    """A CUDA graph replays a launch with its parameters frozen, the merge
-    counters' epoch included: every replay must still merge the parts of a
-    unit the balanced split cut (the last part clears its counter)."""
+    """A CUDA graph replays the call's two launches (the pass over the pages
+    and the programmatic-dependent merge of units the balanced split cut)
+    with their parameters frozen: every replay must write the eager call's
+    output bit for bit, the cut units' rows (which only the merge writes)
+    included."""
     w = wl.WORKLOADS["isd_c64_n4_ctx4096"]
     a = wl.attention_inputs(w)
     eager, st = gpu_attention(a, w.rows_full)
