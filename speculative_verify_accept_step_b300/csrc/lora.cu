@@ -1099,7 +1099,21 @@ LoraPlan plan_for(int M, int K, int N, int r, int grid_cap) {
     // another (an L2 round trip each), so deep splits of few tiles cost a
     // serial chain of ~0.8 us per part
     const double chain = cut ? 0.8 * static_cast<double>((G + skt - 1) / std::max(skt, 1) + 1) : 0.0;
-    const double t = (dp * pl.S + sk_per) * step + (dp ? 3.0 * f : 0.0) +
+    // a CTA whose stream-K share crosses a tile boundary drains a partial
+    // tile in mid-range, and with one accumulator its MMAs wait for that
+    // drain (~4.3 us at 448 tokens); grids that split every tile into whole
+    // shares avoid it (measured: q|k|v 40.1 us at 144 CTAs against 45.6 at
+    // 148, o and down 6 us faster at 128 than at 148)
+    // (shares are shorter than a tile, so a share crosses one boundary at
+    // most; boundary t S is crossed unless a share starts there)
+    bool crosses = false;
+    for (int t = 1; usk > 0 && t < skt && !crosses; ++t) {
+      const long long x = static_cast<long long>(t) * pl.S;
+      const long long c = (x * G + usk - 1) / usk;
+      crosses = c * usk / G != x;
+    }
+    const double straddle = crosses ? 4.3 * f : 0.0;
+    const double t = (dp * pl.S + sk_per) * step + (dp ? 3.0 * f : 0.0) + straddle +
                      (cut ? 2.0 * f + 3.0 + part_mb / (0.1 * G) + chain : (usk ? 3.0 * f : 0.0));
     if (t < best * 0.98) {
       best = t;
