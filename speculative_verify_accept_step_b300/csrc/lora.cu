@@ -43,7 +43,10 @@
 // equal share of the (tile, K step) units of the tiles left over (stream-K);
 // a segment of a left-over tile that a CTA does not hold whole is written as
 // an fp32 partial tile and summed by the fix-up kernel.  No CTA waits for
-// another, and the sums do not depend on timing.
+// another, and the sums do not depend on timing.  The host picks the grid
+// from a cost model of the measured phases (K steps, drains, the fix-up's
+// chain of partials, and a mid-range drain wherever a CTA's share crosses a
+// tile boundary, since one accumulator makes the MMAs wait for it).
 // For the LM head of the fused LM-head + accept call (no adapter, Y = the
 // logits) the epilogue and the fix-up also write the softmax statistics of
 // every token row over each 128-entry tile (TileStat), read back from the
